@@ -1,0 +1,278 @@
+/*
+ * attn_oracle.c -- plain, slow CPU oracle for fused exact attention (fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this code:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * What it computes (FlashAttention-4 pages, "The Asymmetric Hardware Scaling
+ * Wall on NVIDIA Blackwell", the three phases GEMM 1 / Softmax / GEMM 2, and the
+ * functional validation harness, which calls the result "mathematically
+ * exact"): attention is exact, so the oracle is the plain definition
+ *
+ *     s_ij  = scale * sum_d q_id k_jd            (j allowed; causal: j <= i)
+ *     LSE_i = M_i + ln sum_j exp(s_ij - M_i),   M_i = max_j s_ij
+ *     P_ij  = exp(s_ij - LSE_i)
+ *     O_id  = sum_j P_ij v_jd
+ *
+ * with the causal mask q_idx >= kv_idx (top-left, the only form the pages'
+ * simulator prints) and grouped heads: q head h reads kv head floor(h*Hkv/Hq).
+ *
+ * The backward pass is the textbook gradient of that definition (the pages give
+ * none):  dV_j = sum_i P_ij dO_i,  dP_ij = dO_i . v_j,  D_i = dO_i . O_i,
+ *         dS_ij = P_ij (dP_ij - D_i),  dQ_i = scale sum_j dS_ij k_j,
+ *         dK_j = scale sum_i dS_ij q_i  (dK, dV summed over the q heads of a group).
+ *
+ * A second entry point restates the tiled online-softmax loop of the pages'
+ * simulator ("End-to-End Implementation" section): q-tile outer loop, kv-tile
+ * inner loop, running max and sum, accumulator rescale, final O/l.  Mode 0
+ * rescales on every tile as the simulator does; mode 1 is the conditional
+ * rescale of the pages' key contribution #2 (skip unless the running max grows
+ * by more than log2(256) = 8.0), taken in the base-2 domain.  It exists to pin
+ * that the tiled algorithm reaches the plain definition.
+ *
+ * Tensors are dense row-major [B, H, S, D] (the simulator's docstring layout),
+ * LSE is [B, Hq, Sq], natural log.  Every routine returns 0 on success and a
+ * negative value on a bad argument.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_version(void) { return 1; }
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+/* Grouped heads: contiguous groups of Hq/Hkv query heads share one kv head. */
+static int kv_head_of(int h, int Hq, int Hkv) { return (int)(((long long)h * Hkv) / Hq); }
+
+/* Number of keys row i may attend to (top-left causal: j <= i). */
+static long allowed_keys(long i, long Sk, int causal) {
+  if (!causal) return Sk;
+  return (i + 1 < Sk) ? i + 1 : Sk;
+}
+
+static double dot(const double* a, const double* b, long D) {
+  double acc = 0.0;
+  for (long d = 0; d < D; ++d) acc += a[d] * b[d];
+  return acc;
+}
+
+static int check_dims(int B, int Hq, int Hkv, int Sq, int Sk, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || D < 1) return -1;
+  if (Hq % Hkv != 0) return -2;
+  return 0;
+}
+
+/*
+ * Forward pass of one query row from the definition.  s is scratch of Sk
+ * doubles.  Writes D values of O and the row's LSE.
+ */
+static void fwd_one_row(const double* q_row, const double* k_head, const double* v_head,
+                        long Sk, long D, long n_allowed, double scale, double* s,
+                        double* o_row, double* lse_out) {
+  if (n_allowed <= 0) { /* fully masked row: empty softmax */
+    for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+    *lse_out = -INFINITY;
+    return;
+  }
+  double M = -INFINITY;
+  for (long j = 0; j < n_allowed; ++j) {
+    s[j] = scale * dot(q_row, k_head + j * D, D);
+    if (s[j] > M) M = s[j];
+  }
+  double sum = 0.0;
+  for (long j = 0; j < n_allowed; ++j) sum += exp(s[j] - M);
+  const double lse = M + log(sum);
+  for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+  for (long j = 0; j < n_allowed; ++j) {
+    const double p = exp(s[j] - lse);
+    const double* vj = v_head + j * D;
+    for (long d = 0; d < D; ++d) o_row[d] += p * vj[d];
+  }
+  *lse_out = lse;
+  (void)Sk;
+}
+
+/*
+ * Forward for a list of rows.  rows[r] is a flat row index (b*Hq + h)*Sq + i.
+ * o_rows is [n_rows, D], lse_rows is [n_rows].
+ */
+int oracle_fwd_rows(const double* q, const double* k, const double* v, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int D, int causal, double scale, const int64_t* rows,
+                    int64_t n_rows, double* o_rows, double* lse_rows) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  const long total = (long)B * Hq * Sq;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= total) return -3;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n_rows; ++r) {
+      const long flat = (long)rows[r];
+      const long i = flat % Sq;
+      const long bh = flat / Sq;
+      const long b = bh / Hq, h = bh % Hq;
+      const long hk = kv_head_of((int)h, Hq, Hkv);
+      const double* q_row = q + flat * D;
+      const double* k_head = k + ((b * Hkv + hk) * (long)Sk) * D;
+      const double* v_head = v + ((b * Hkv + hk) * (long)Sk) * D;
+      fwd_one_row(q_row, k_head, v_head, Sk, D, allowed_keys(i, Sk, causal), scale, s,
+                  o_rows + r * D, lse_rows + r);
+    }
+    free(s);
+  }
+  return 0;
+}
+
+/* Full forward: O [B,Hq,Sq,D], LSE [B,Hq,Sq]. */
+int oracle_fwd(const double* q, const double* k, const double* v, int B, int Hq, int Hkv, int Sq,
+               int Sk, int D, int causal, double scale, double* o, double* lse) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  const long total = (long)B * Hq * Sq;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (long flat = 0; flat < total; ++flat) {
+      const long i = flat % Sq;
+      const long bh = flat / Sq;
+      const long b = bh / Hq, h = bh % Hq;
+      const long hk = kv_head_of((int)h, Hq, Hkv);
+      fwd_one_row(q + flat * D, k + ((b * Hkv + hk) * (long)Sk) * D,
+                  v + ((b * Hkv + hk) * (long)Sk) * D, Sk, D, allowed_keys(i, Sk, causal),
+                  scale, s, o + flat * D, lse + flat);
+    }
+    free(s);
+  }
+  return 0;
+}
+
+/*
+ * Backward from the definition for a list of kv-head units u = b*Hkv + hk.
+ * For each unit it writes dK, dV of that kv head and dQ, O, LSE of every q head
+ * in its group; other slices of the (full-size) outputs are left untouched.
+ * O and LSE come from this oracle's own forward.
+ */
+int oracle_bwd_units(const double* q, const double* k, const double* v, const double* dO, int B,
+                     int Hq, int Hkv, int Sq, int Sk, int D, int causal, double scale,
+                     const int64_t* units, int64_t n_units, double* dq, double* dk, double* dv,
+                     double* o, double* lse) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  for (int64_t u = 0; u < n_units; ++u)
+    if (units[u] < 0 || units[u] >= (int64_t)B * Hkv) return -3;
+  const int g = Hq / Hkv;
+  double* delta = (double*)malloc(sizeof(double) * (size_t)(Sq > 0 ? Sq : 1) * (size_t)g);
+  if (!delta) return -4;
+
+  for (int64_t u = 0; u < n_units; ++u) {
+    const long b = (long)(units[u] / Hkv), hk = (long)(units[u] % Hkv);
+    const double* k_head = k + ((b * Hkv + hk) * (long)Sk) * D;
+    const double* v_head = v + ((b * Hkv + hk) * (long)Sk) * D;
+    double* dk_head = dk + ((b * Hkv + hk) * (long)Sk) * D;
+    double* dv_head = dv + ((b * Hkv + hk) * (long)Sk) * D;
+
+    /* Pass 1, per query row: O, LSE, D_i = dO_i . O_i, dQ_i. */
+    for (int gi = 0; gi < g; ++gi) {
+      const long h = hk * g + gi;
+      const long base = (b * Hq + h) * (long)Sq;
+#pragma omp parallel
+      {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long i = 0; i < Sq; ++i) {
+          const long na = allowed_keys(i, Sk, causal);
+          const double* qi = q + (base + i) * D;
+          const double* doi = dO + (base + i) * D;
+          double* oi = o + (base + i) * D;
+          double* dqi = dq + (base + i) * D;
+          fwd_one_row(qi, k_head, v_head, Sk, D, na, scale, s, oi, lse + base + i);
+          const double Di = dot(doi, oi, D);
+          delta[gi * (long)Sq + i] = Di;
+          for (long d = 0; d < D; ++d) dqi[d] = 0.0;
+          for (long j = 0; j < na; ++j) {
+            const double p = exp(s[j] - lse[base + i]);
+            const double dp = dot(doi, v_head + j * D, D);
+            const double ds = p * (dp - Di);
+            const double* kj = k_head + j * D;
+            for (long d = 0; d < D; ++d) dqi[d] += scale * ds * kj[d];
+          }
+        }
+        free(s);
+      }
+    }
+
+    /* Pass 2, per key row: dK_j, dV_j summed over the group's q heads and rows. */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long j = 0; j < Sk; ++j) {
+      double* dkj = dk_head + j * D;
+      double* dvj = dv_head + j * D;
+      for (long d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+      const double* kj = k_head + j * D;
+      const double* vj = v_head + j * D;
+      for (int gi = 0; gi < g; ++gi) {
+        const long h = hk * g + gi;
+        const long base = (b * Hq + h) * (long)Sq;
+        for (long i = causal ? j : 0; i < Sq; ++i) {
+          const double* qi = q + (base + i) * D;
+          const double* doi = dO + (base + i) * D;
+          const double sij = scale * dot(qi, kj, D);
+          const double p = exp(sij - lse[base + i]);
+          const double dp = dot(doi, vj, D);
+          const double ds = p * (dp - delta[gi * (long)Sq + i]);
+          for (long d = 0; d < D; ++d) {
+            dkj[d] += scale * ds * qi[d];
+            dvj[d] += p * doi[d];
+          }
+        }
+      }
+    }
+  }
+  free(delta);
+  return 0;
+}
+
+/* ---- tiled online-softmax restatement, fp64 and fp32 ---- */
+#define REAL double
+#define EXP exp
+#define EXP2 exp2
+#define LOG log
+#define LOG2 log2
+#define TILED_NAME oracle_tiled_fwd_f64
+#include "tiled_body.h"
+#undef REAL
+#undef EXP
+#undef EXP2
+#undef LOG
+#undef LOG2
+#undef TILED_NAME
+
+#define REAL float
+#define EXP expf
+#define EXP2 exp2f
+#define LOG logf
+#define LOG2 log2f
+#define TILED_NAME oracle_tiled_fwd_f32
+#include "tiled_body.h"
