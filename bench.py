@@ -1,0 +1,425 @@
+"""Throughput benchmark of the fused attention path on GB300.
+
+One step = one training-style pass of the whole hot path over one batch:
+fa_fwd (causal) followed by fa_bwd (causal, atomic dQ) on the training-scale
+workload B=4, Hq=Hkv=16, S=2048, D=128, bf16 (synthetic N(0,1) inputs).
+FLOPs per step follow the measurement convention: 4*B*Hq*Sq*Sk*D forward,
+halved for causal, plus 2.5x that for the backward pass.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (one rank per GPU)
+
+With N > 1 every rank runs its own batch of the same workload (independent
+units, no collective on the data path); the timing is the max over ranks and
+``value`` counts the FLOPs of all ranks ("weak" scaling).
+
+``--impl reference`` times the fp64 CPU oracle as it stands, on a bounded
+sample of the same workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPs/s (BF16, 1×GB300) and % of tensor-core peak"
+UNIT = "TFLOP/s"
+WORKLOAD = synth.TRAIN  # B=4, Hq=Hkv=16, S=2048, D=128, causal
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def step_flops(w: synth.Workload) -> float:
+    return w.flops(backward=False) + w.flops(backward=True)
+
+
+def config_dict(w: synth.Workload) -> dict:
+    return {"workload": f"attention fwd+bwd, {'causal' if w.causal else 'non-causal'}, B={w.B} "
+                        f"Hq={w.Hq} Hkv={w.Hkv} S={w.Sq} D={w.D} bf16",
+            "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+            "causal": w.causal, "dq_mode": "atomic",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured (MEASURED_PEAKS.json)"
+    return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_blackwell_tiled_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/traffic.json),
+    or None when absent or taken on different kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = sorted(float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit())
+        mx = max((float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[5:9])
+                          if v.lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float across the process group (identity when world == 1)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(w: synth.Workload, budget_s: float = 12.0, max_heads: int | None = None):
+    """Time the fp64 oracle (forward + backward of whole kv heads) on a bounded
+    sample of the workload.  Returns (TFLOP/s in the FLOP convention, cores,
+    sample description, seconds)."""
+    import numpy as np
+    import oracle
+
+    q, k, v, do = synth.make_inputs(w, with_do=True)
+    cores = oracle.max_threads()
+    n_units = w.B * w.Hkv
+    per_unit_flops = step_flops(w) / n_units
+    done, t0 = 0, time.perf_counter()
+    cap = n_units if max_heads is None else min(n_units, max_heads)
+    while done < cap:
+        oracle.bwd(q, k, v, do, w.causal, w.softmax_scale, units=[done])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    value = per_unit_flops * done / dt / 1e12
+    sample = (f"fp64 oracle forward+backward of {done} of {n_units} kv heads "
+              f"(B*Hkv units) of the workload, {dt:.1f} s; FLOPs counted by the same convention")
+    return value, cores, sample, dt
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import exact_attention_blackwell_tiled_gb300 as fa
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD.with_(seed=WORKLOAD.seed + 1000 * rank)  # each rank its own batch
+    q, k, v, do = synth.make_inputs(w, with_do=True)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    scale = w.softmax_scale
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(time_kernels=None):
+        launches = 0
+        if time_kernels is not None:
+            fa.set_timing_events(*time_kernels[0])
+        fa.fwd(qd, kd, vd, causal=w.causal, scale=scale, out=o, lse=lse)
+        launches += fa.last_launch_count()
+        if time_kernels is not None:
+            fa.set_timing_events(*time_kernels[1])
+        fa.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=scale, workspace=ws, dq=dq, dk=dk,
+               dv=dv)
+        launches += fa.last_launch_count()
+        return launches
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    launches = 0
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush outside the timed interval
+            e = ev[i]
+            e[0].record(stream)
+            launches += step(time_kernels=((e[2], e[3]), (e[4], e[5])))
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    fwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    bwd_main_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    total_ms_local = sum(step_ms)
+    total_ms = max_over_ranks(total_ms_local, world, dev)
+    ms_per_step = total_ms / args.steps
+    flops = step_flops(w)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_f, bwd_f = w.flops(False), w.flops(True)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    bwd_avg = sum(bwd_main_ms) / len(bwd_main_ms)
+    bwd_tf = bwd_f / (bwd_avg * 1e-3) / 1e12
+    fwd_tf = fwd_f / (fwd_avg * 1e-3) / 1e12
+    if bwd_avg >= fwd_avg:
+        dom, dom_tf, dom_flops = "bwd_main<128>", bwd_tf, bwd_f
+    else:
+        dom, dom_tf, dom_flops = "fwd_kernel<128>", fwd_tf, fwd_f
+    roofline = {"bound": "tensor", "achieved": round(dom_tf, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(dom_tf / peak, 4), "traffic": profiled_traffic(dom),
+                "kernel": dom, "flops_per_launch": dom_flops,
+                "peak_source": f"bf16_tflops burst, {peak_src}"}
+    clocks = clk.summary()
+
+    # end-to-end through the public API: pinned host inputs -> device -> fwd+bwd -> host grads
+    e2e = None
+    if rank == 0 or world > 1:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
+        n_e2e = max(3, min(args.steps, 50))
+        for it in range(n_e2e + 2):
+            if it == 2:
+                torch.cuda.synchronize(dev)
+                t_e0 = torch.cuda.Event(enable_timing=True)
+                t_e1 = torch.cuda.Event(enable_timing=True)
+                t_e0.record(stream)
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            dod.copy_(hdo, non_blocking=True)
+            fa.fwd(qd, kd, vd, causal=w.causal, scale=scale, out=o, lse=lse)
+            fa.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=scale, workspace=ws, dq=dq,
+                   dk=dk, dv=dv)
+            for hdst, dsrc in zip(out_h, (dq, dk, dv)):
+                hdst.copy_(dsrc, non_blocking=True)
+        t_e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(t_e0.elapsed_time(t_e1) / n_e2e, world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+        d2h = sum(t.numel() * t.element_size() for t in out_h)
+        e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4)}
+
+    assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
+
+    extra = {"fwd_tflops": round(fwd_tf, 1), "fwd_ms": round(fwd_avg, 4),
+             "bwd_main_tflops": round(bwd_tf, 1), "bwd_main_ms": round(bwd_avg, 4),
+             "bwd_total_flops_tflops_incl_pre_post": None,
+             "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak}
+    if args.sweep and rank == 0:
+        extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, _ = cpu_oracle_sample(w, budget_s=args.cpu_budget)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
+            "config": config_dict(w), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks, "extra": extra}
+    print(json.dumps(line), flush=True)
+
+
+def fwd_sweep(fa, dev, peak, iters=10):
+    """Forward-only TFLOP/s over the sequence-length sweep (16k tokens per batch)."""
+    import torch
+    out = []
+    for S in synth.SWEEP_S:
+        for D in (64, 128):
+            for causal in (False, True):
+                w = synth.sweep(S, D, causal)
+                q, k, v = (torch.randn(w.B, w.Hq, S, D, device=dev, dtype=torch.bfloat16)
+                           for _ in range(3))
+                o = torch.empty_like(q)
+                lse = torch.empty((w.B, w.Hq, S), dtype=torch.float32, device=dev)
+                for _ in range(3):
+                    fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+                torch.cuda.synchronize(dev)
+                t = []
+                for _ in range(iters):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    fa.set_timing_events(e0, e1)
+                    fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+                    t.append((e0, e1))
+                torch.cuda.synchronize(dev)
+                ms = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
+                tf = w.flops() / (ms * 1e-3) / 1e12
+                out.append({"S": S, "D": D, "B": w.B, "causal": causal, "ms": round(ms, 4),
+                            "tflops": round(tf, 1), "frac": round(tf / peak, 4)})
+                del q, k, v, o, lse
+    return out
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return  # the CPU oracle runs once, on rank 0
+    w = WORKLOAD
+    steps, per_step = [], []
+    budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        v, cores, sample, dt = cpu_oracle_sample(w, budget_s=budget, max_heads=1)
+        if i >= args.warmup:
+            steps.append(v)
+            per_step.append(dt)
+    value = sum(steps) / len(steps)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000 * sum(per_step) / len(per_step), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep", action="store_true", help="also time the forward S/D sweep")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for the baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

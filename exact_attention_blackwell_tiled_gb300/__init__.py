@@ -1,0 +1,185 @@
+"""GB300 (sm_103a) fused exact attention: thin Python binding over libfa.so.
+
+Every computation runs in the library's CUDA kernels; this module only checks
+tensor properties, allocates outputs with torch and passes raw pointers plus the
+current CUDA stream through the C ABI declared in ``include/fa.h``.  There is no
+CPU or eager fallback: if the library is missing or a tensor is not a
+contiguous bf16 CUDA tensor, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
+                3: "FA_ERR_MISALIGNED", 4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA",
+                6: "FA_ERR_TIMEOUT"}
+
+#: every symbol include/fa.h declares
+EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
+           "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events")
+
+_LIB = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def _bind(lib):
+    vp, i, f, sz, i64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                         ctypes.c_int64)
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_fwd_status.argtypes = [vp]
+    lib.fa_fwd_status.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, i,
+                           vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_status.argtypes = [vp, vp]
+    lib.fa_bwd_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_exp2_test.argtypes = [vp, vp, i64, i, vp]
+    lib.fa_exp2_test.restype = i
+    lib.fa_last_launch_count.argtypes = []
+    lib.fa_last_launch_count.restype = i
+    lib.fa_set_timing_events.argtypes = [vp, vp]
+    lib.fa_set_timing_events.restype = i
+    return lib
+
+
+def lib():
+    """The loaded libfa.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        _LIB = _bind(ctypes.CDLL(LIB_PATH))
+    return _LIB
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, S, D]")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, S, D]")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: float | None = None, out: torch.Tensor | None = None,
+        lse: torch.Tensor | None = None, stream=None):
+    """Forward attention. q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA.
+
+    Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] fp32, natural log).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                      int(bool(causal)), float(scale), _stream(stream))
+    if rc != FA_OK:
+        raise FAError("fa_fwd", rc)
+    return out, lse
+
+
+def bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, deterministic=False) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(bool(deterministic))))
+
+
+def bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+        deterministic: bool = False, workspace: torch.Tensor | None = None,
+        dq=None, dk=None, dv=None, stream=None):
+    """Backward attention. Returns (dq, dk, dv) bf16, same shapes as q, k, v."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check(t, n)
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, deterministic)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                      _ptr(dv), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                      _ptr(workspace), workspace.numel(), int(bool(deterministic)),
+                      _stream(stream))
+    if rc != FA_OK:
+        raise FAError("fa_bwd", rc)
+    return dq, dk, dv
+
+
+def fwd_status(stream=None) -> int:
+    """Synchronise and return (then clear) the forward kernels' timeout record."""
+    return int(lib().fa_fwd_status(_stream(stream)))
+
+
+def bwd_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(lib().fa_bwd_status(_ptr(workspace), _stream(stream)))
+
+
+def exp2_test(x: torch.Tensor, which: int, stream=None) -> torch.Tensor:
+    """2^x through the kernel's MUFU path (which=0) or polynomial path (which=1)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous fp32 CUDA tensor")
+    y = torch.empty_like(x)
+    rc = lib().fa_exp2_test(_ptr(x), _ptr(y), x.numel(), int(which), _stream(stream))
+    if rc != FA_OK:
+        raise FAError("fa_exp2_test", rc)
+    return y
+
+
+def last_launch_count() -> int:
+    return int(lib().fa_last_launch_count())
+
+
+def set_timing_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:
+    """Record ``start``/``stop`` around the main kernel of the next fwd/bwd call
+    made by this thread (events must be created with timing enabled)."""
+    ps = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    pe = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    rc = lib().fa_set_timing_events(ps, pe)
+    if rc != FA_OK:
+        raise FAError("fa_set_timing_events", rc)

@@ -1,0 +1,279 @@
+// fa_api.cu -- the extern "C" boundary of libfa.so: argument validation, tensor
+// maps, workspace layout and dispatch to the kernels.  See include/fa.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+namespace {
+
+thread_local int t_launches = 0;
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_stop = nullptr;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape rules shared by the forward and backward entry points.
+int check_shape(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 0 || Sk < 1) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  // TMA coordinates and element counts are 32-bit signed in the kernels.
+  const long long bh = (long long)B * Hq;
+  if (bh > (1LL << 30) || (long long)Sq > (1LL << 30) || (long long)Sk > (1LL << 30))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+int check_device() {
+  int dev;
+  DeviceInfo info;
+  if (!current_device(&dev, &info)) return FA_ERR_CUDA;
+  if (info.cc_major != 10 || info.cc_minor != 3) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+void note_launches(int n) { t_launches += n; }
+
+void record_timing(bool stop, cudaStream_t stream) {
+  if (!t_ev_start || !t_ev_stop) return;
+  if (!stop) {
+    cudaEventRecord(t_ev_start, stream);
+  } else {
+    cudaEventRecord(t_ev_stop, stream);
+    t_ev_start = t_ev_stop = nullptr;
+  }
+}
+
+bool current_device(int* dev, DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int d;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[d]) {
+    DeviceInfo info;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+      return false;
+    cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, d);
+    cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    info.smem_optin = (size_t)v;
+    cache[d] = info;
+    have[d] = true;
+  }
+  *dev = d;
+  *out = cache[d];
+  return true;
+}
+
+bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool bwd_layout(int B, int Hq, int Sq, int D, BwdLayout* L) {
+  // A 256-byte header holding the status word comes first, so fa_bwd_status can
+  // find it without knowing the sizes.
+  const size_t nq = (size_t)((Sq + kTile - 1) / kTile);
+  const size_t rows = (size_t)B * Hq * nq * kTile;
+  L->off_status = 0;
+  L->off_dq_acc = 256;
+  L->off_delta = align256(L->off_dq_acc + rows * D * sizeof(float));
+  L->off_lse2 = align256(L->off_delta + rows * sizeof(float));
+  L->off_sem = align256(L->off_lse2 + rows * sizeof(float));
+  L->total = align256(L->off_sem + (size_t)B * Hq * (nq > 0 ? nq : 1) * sizeof(int));
+  return true;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_last_launch_count(void) { return t_launches; }
+
+int fa_set_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return FA_ERR_INVALID_ARG;
+  t_ev_start = static_cast<cudaEvent_t>(start_event);
+  t_ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream) {
+  t_launches = 0;
+  int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
+  if (rc) return rc;
+  if (Sq == 0) return FA_OK;  // nothing to read or write; q, o, lse may be null
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if ((rc = check_device())) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bsd(&tq, q, B * Hq, Sq, D) || !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) ||
+      !make_tmap_bsd(&tv, v, B * Hkv, Sk, D))
+    return FA_ERR_CUDA;
+  FwdArgs a{};
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_qtiles = (Sq + kTile - 1) / kTile;
+  a.n_units = B * Hq * a.n_qtiles;
+  return launch_fwd(tq, tk, tv, a, D, static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_status(fa_stream_t stream) { return fwd_status_take(static_cast<cudaStream_t>(stream)); }
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
+  (void)deterministic;
+  if (check_shape(B, Hq, Hkv, Sq, Sk, D, 1.0f) != FA_OK) return 0;
+  BwdLayout L;
+  bwd_layout(B, Hq, Sq, D, &L);
+  return L.total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+           int deterministic, fa_stream_t stream) {
+  t_launches = 0;
+  int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
+  if (rc) return rc;
+  // With Sq == 0 the query-side tensors are empty and may be null; dk and dv
+  // are still written (as zeros).
+  const bool has_q = Sq > 0;
+  if (!k || !v || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (has_q && (!q || !o || !dO || !lse || !dq)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  if (has_q && (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+                !aligned16(dq)))
+    return FA_ERR_MISALIGNED;
+  BwdLayout L;
+  bwd_layout(B, Hq, Sq, D, &L);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < L.total)
+    return FA_ERR_WORKSPACE;
+  if ((rc = check_device())) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  // Sq == 0 still needs dk = dv = 0: the kernels handle it with zero q tiles.
+  // With no q tiles the q / dO maps are never used; they are built over k.
+  const void* q_map = has_q ? q : k;
+  const void* do_map = has_q ? dO : k;
+  const int bh_map = has_q ? B * Hq : B * Hkv;
+  const int sq_map = has_q ? Sq : Sk;
+  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D) || !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) ||
+      !make_tmap_bsd(&tv, v, B * Hkv, Sk, D) || !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D))
+    return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdArgs a{};
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(ws + L.off_dq_acc);
+  a.delta = reinterpret_cast<float*>(ws + L.off_delta);
+  a.lse2 = reinterpret_cast<float*>(ws + L.off_lse2);
+  a.sem = reinterpret_cast<int*>(ws + L.off_sem);
+  a.status = reinterpret_cast<int*>(ws + L.off_status);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.D = D;
+  a.n_qtiles = (Sq + kTile - 1) / kTile;
+  a.Sq_pad = a.n_qtiles * kTile;
+  a.n_ktiles = (Sk + kTile - 1) / kTile;
+  a.n_units = B * Hkv * a.n_ktiles;
+  a.causal = causal ? 1 : 0;
+  a.deterministic = deterministic ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_status(const void* workspace, fa_stream_t stream) {
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return v == 0 ? FA_OK : v;
+}
+
+int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream) {
+  t_launches = 0;
+  if (n < 0 || (which != 0 && which != 1)) return FA_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !y)) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_exp2_test(x, y, n, which, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

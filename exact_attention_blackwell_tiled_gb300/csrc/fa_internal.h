@@ -1,0 +1,85 @@
+// fa_internal.h -- declarations shared by the host-side translation units of
+// libfa.so (argument structs, per-device cache, kernel launchers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  size_t smem_optin = 0;
+};
+
+// Cached attributes of the current device; false if no device is usable.
+bool current_device(int* dev, DeviceInfo* info);
+
+// Encodes a 3-D tensor map over a [BH, S, D] bf16 tensor with 128-row x
+// 64-column boxes and the 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D);
+
+struct FwdArgs {
+  void* o;
+  float* lse;
+  int* status;
+  int B, Hq, Hkv, Sq, Sk;
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  int n_qtiles;
+  int n_units;
+  int chunk;  // > 0: CTA c takes units [c*chunk, (c+1)*chunk); 0: round robin
+};
+
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const FwdArgs& a, int D, cudaStream_t stream);
+int fwd_status_take(cudaStream_t stream);
+int launch_exp2_test(const float* x, float* y, int64_t n, int which, cudaStream_t stream);
+
+struct BwdArgs {
+  const void* o;
+  const void* dO;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;   // [B, Hq, Sq_pad, D]
+  float* delta;    // [B, Hq, Sq_pad]
+  float* lse2;     // [B, Hq, Sq_pad]
+  int* sem;        // [B, Hq, n_qtiles]
+  int* status;     // [1]
+  int B, Hq, Hkv, Sq, Sk, D;
+  int Sq_pad;
+  int causal;
+  int deterministic;
+  float scale;
+  float scale_log2;
+  int n_qtiles;
+  int n_ktiles;
+  int n_units;
+};
+
+struct BwdLayout {
+  size_t off_dq_acc, off_delta, off_lse2, off_sem, off_status, total;
+};
+bool bwd_layout(int B, int Hq, int Sq, int D, BwdLayout* L);
+
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+
+void note_launches(int n);
+
+// Events requested by fa_set_timing_events for the next main-kernel launch on
+// this thread; record_timing(true/false) records start/stop and clears after stop.
+void record_timing(bool stop, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,141 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused exact-attention library libfa.so.
+ *
+ * The operation is exact scaled-dot-product attention as the FlashAttention-4
+ * pages state it (blog page "FlashAttention-4 Guide", section "The Asymmetric
+ * Hardware Scaling Wall on NVIDIA Blackwell": GEMM 1  S = QK^T * scale, the
+ * softmax  P = exp(S - m)/l,  GEMM 2  O = PV; the simulator's signature in
+ * "End-to-End Implementation" takes q, k, v, a causal flag and a scale).  The
+ * log-sum-exp output and the backward pass are the plain mathematics of that
+ * definition:
+ *
+ *   s_ij = scale * q_i . k_j   (causal: only j <= i, top-left)
+ *   LSE_i = ln sum_j exp(s_ij),  P_ij = exp(s_ij - LSE_i),  O_i = sum_j P_ij v_j
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - dO_i . O_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i
+ *
+ * Layout: every tensor is dense row-major [B, H, S, D] (the simulator's
+ * docstring layout); H = Hq for q, o, dO, dq and H = Hkv for k, v, dk, dv.
+ * q/k/v/o/dO/dq/dk/dv are bf16 (raw 16-bit storage), lse is fp32 [B, Hq, Sq] in
+ * natural log.  Grouped heads: Hq % Hkv == 0 and q head h reads kv head
+ * floor(h * Hkv / Hq).  D must be 64 or 128.
+ *
+ * Ownership: the caller owns every buffer (all device pointers), including the
+ * backward workspace.  The library never allocates device memory; it keeps a
+ * small host-side cache of per-device attributes.  All calls are asynchronous
+ * on `stream` (0 = legacy default stream); results are valid after the stream
+ * is synchronised.
+ *
+ * Errors: arguments are validated on the host before anything is launched; on
+ * a validation error nothing is written and a status code is returned.  Launch
+ * failures return FA_ERR_CUDA.  Device-side waits carry an iteration/time cap;
+ * one that runs out records FA_ERR_TIMEOUT in a status word and the kernel
+ * returns early (fa_fwd_status / fa_bwd_status report it).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0, non-finite scale */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 / 128, or a device that is not sm_103 */
+  FA_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned (TMA requirement) */
+  FA_ERR_WORKSPACE = 4,   /* backward workspace missing, misaligned or too small */
+  FA_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_TIMEOUT = 6      /* a device-side wait ran out (reported by the status calls) */
+} fa_status;
+
+/* An opaque CUDA stream (cudaStream_t). */
+typedef void* fa_stream_t;
+
+/*
+ * Forward pass: o = softmax(scale * q k^T [causal]) v and lse.
+ *   q   [B, Hq,  Sq, D] bf16      k, v [B, Hkv, Sk, D] bf16
+ *   o   [B, Hq,  Sq, D] bf16 out  lse  [B, Hq, Sq] fp32 out (natural log)
+ * Sizes: B, Hq, Hkv, Sk >= 1; Sq >= 0 (Sq == 0 is a no-op); D in {64, 128};
+ * scale finite.  causal != 0 applies the top-left mask q_idx >= kv_idx, which
+ * leaves no row empty when Sk >= 1.  Pointers must be non-null and 16-byte
+ * aligned (when Sq == 0 nothing is checked, read or written).  Output rows are
+ * written exactly once; nothing outside them is touched.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, returns FA_OK or FA_ERR_TIMEOUT if any forward launch on
+ * this device since the previous call recorded a timed-out wait, and clears the
+ * record.  FA_ERR_CUDA if the synchronisation itself fails.
+ */
+int fa_fwd_status(fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes (0 on bad sizes).  The
+ * workspace holds an fp32 dQ accumulator [B, Hq, ceil(Sq/128)*128, D], the
+ * per-row dot products D_i = dO_i . O_i and LSE*log2(e) (fp32 [B, Hq, padded
+ * Sq]), the deterministic mode's per-(b, h, q-tile) semaphores and a status
+ * word.  It needs no initialisation: fa_bwd clears what it uses.
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
+
+/*
+ * Backward pass: dq, dk, dv of L with dL/dO = dO, given the forward's o and lse.
+ *   q, o, dO, dq [B, Hq, Sq, D] bf16;  k, v, dk, dv [B, Hkv, Sk, D] bf16;
+ *   lse [B, Hq, Sq] fp32 (natural log, as written by fa_fwd).
+ * dq, dk, dv are overwritten (not accumulated); dk and dv sum over the q heads
+ * of a group.  workspace: device memory of at least
+ * fa_bwd_workspace_bytes(...) bytes, 256-byte aligned.  deterministic != 0
+ * serialises the dQ accumulation in a fixed kv-tile order through semaphores,
+ * so repeated runs give identical bits; otherwise dQ partials are added with
+ * fp32 atomics (the last bits may differ between runs).  Same size and
+ * pointer rules as fa_fwd, except that Sq == 0 is not a no-op: dk and dv are
+ * then zero (q, o, dO, lse and dq may be null).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+           int deterministic, fa_stream_t stream);
+
+/*
+ * Synchronises `stream` and returns the status the last fa_bwd recorded in
+ * `workspace` (FA_OK or FA_ERR_TIMEOUT); FA_ERR_CUDA if the sync fails.
+ */
+int fa_bwd_status(const void* workspace, fa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(int status);
+
+/*
+ * Test hook for the exponential split of the forward softmax (FlashAttention-4
+ * pages, key contribution #2: a degree-3 polynomial on the FMA units run beside
+ * the MUFU exp2).  Writes y[i] = 2^x[i] computed the way the kernel does:
+ * which = 0 the hardware ex2.approx path, which = 1 the polynomial path.
+ * x, y: device fp32 arrays of n elements.  Inputs below -125 give 2^-125 on the
+ * polynomial path (the kernel's clamp), values above 64 are not supported.
+ */
+int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream);
+
+/* Number of kernels the last fa_fwd / fa_bwd call on this thread launched. */
+int fa_last_launch_count(void);
+
+/*
+ * Measurement hook.  Records two caller-owned CUDA events (cudaEvent_t, passed
+ * as void*) on the call's stream immediately before and after the main kernel
+ * of the NEXT fa_fwd or fa_bwd issued by this thread (the forward kernel, or
+ * the backward's main kernel without its preprocess / convert kernels), then
+ * forgets them.  Passing two nulls cancels a pending request.  Returns
+ * FA_ERR_INVALID_ARG if exactly one of the two is null.
+ */
+int fa_set_timing_events(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

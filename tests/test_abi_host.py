@@ -1,0 +1,112 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import exact_attention_blackwell_tiled_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+P16 = ctypes.c_void_p(16 * 1024)  # aligned, never dereferenced: validation fails first
+P17 = ctypes.c_void_p(16 * 1024 + 1)
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return fa.lib()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert declared == set(fa.EXPORTS), declared ^ set(fa.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), f"libfa.so does not export {name}"
+
+
+def test_status_strings(L):
+    for code, name in fa.STATUS_NAMES.items():
+        assert L.fa_status_string(code).decode() == name
+    assert L.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+
+
+def _fwd(L, q=P16, k=P16, v=P16, o=P16, lse=P16, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, D=64, causal=0,
+         scale=0.125):
+    return L.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, None)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    assert _fwd(L, q=None) == 1
+    assert _fwd(L, lse=None) == 1
+    assert _fwd(L, B=0) == 1
+    assert _fwd(L, Hq=0) == 1
+    assert _fwd(L, Sk=0) == 1
+    assert _fwd(L, Sq=-1) == 1
+    assert _fwd(L, Hq=3, Hkv=2) == 1
+    assert _fwd(L, scale=float("nan")) == 1
+    assert _fwd(L, scale=float("inf")) == 1
+    assert _fwd(L, D=96) == 2
+    assert _fwd(L, D=256) == 2
+    assert _fwd(L, q=P17) == 3
+    assert _fwd(L, o=P17) == 3
+    # Sq == 0 is a no-op that needs no device
+    assert _fwd(L, Sq=0) == 0
+    assert L.fa_last_launch_count() == 0
+
+
+def test_bwd_rejects_bad_arguments(L):
+    need = L.fa_bwd_workspace_bytes(1, 2, 2, 8, 8, 64, 0)
+    assert need > 0
+
+    def call(ws=P16, ws_bytes=need, **kw):
+        a = dict(q=P16, k=P16, v=P16, o=P16, do=P16, lse=P16, dq=P16, dk=P16, dv=P16, B=1, Hq=2,
+                 Hkv=2, Sq=8, Sk=8, D=64, causal=0, scale=0.125, det=0)
+        a.update(kw)
+        return L.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                        a["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["D"], a["causal"],
+                        a["scale"], ws, ws_bytes, a["det"], None)
+
+    assert call(dq=None) == 1
+    assert call(Hq=4, Hkv=3) == 1
+    assert call(D=80) == 2
+    assert call(dk=P17) == 3
+    assert call(ws=None) == 4
+    assert call(ws_bytes=need - 1) == 4
+    assert call(ws=ctypes.c_void_p(16 * 1024 + 16)) == 4  # workspace must be 256-byte aligned
+
+
+def test_workspace_size(L):
+    assert L.fa_bwd_workspace_bytes(0, 1, 1, 8, 8, 64, 0) == 0
+    assert L.fa_bwd_workspace_bytes(1, 1, 1, 8, 8, 72, 0) == 0
+    small = L.fa_bwd_workspace_bytes(1, 2, 2, 100, 100, 64, 0)
+    big = L.fa_bwd_workspace_bytes(2, 16, 16, 8192, 8192, 128, 1)
+    assert 0 < small < big
+    # fp32 dQ accumulator dominates: B*Hq*Sq_pad*D*4
+    assert big >= 2 * 16 * 8192 * 128 * 4
+    assert big % 256 == 0
+
+
+def test_exp2_hook_validation(L):
+    assert L.fa_exp2_test(None, None, 0, 0, None) == 0
+    assert L.fa_exp2_test(None, None, -1, 0, None) == 1
+    assert L.fa_exp2_test(P16, P16, 4, 2, None) == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fa.fwd(x, x, x)
