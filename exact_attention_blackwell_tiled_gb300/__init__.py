@@ -178,6 +178,9 @@ def last_launch_count() -> int:
 def set_timing_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:
     """Record ``start``/``stop`` around the main kernel of the next fwd/bwd call
     made by this thread (events must be created with timing enabled)."""
+    for e in (start, stop):
+        if e is not None and e.cuda_event == 0:
+            e.record()  # torch creates the CUDA event lazily, on its first record
     ps = ctypes.c_void_p(start.cuda_event) if start is not None else None
     pe = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
     rc = lib().fa_set_timing_events(ps, pe)

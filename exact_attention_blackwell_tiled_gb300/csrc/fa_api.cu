@@ -98,12 +98,12 @@ bool current_device(int* dev, DeviceInfo* out) {
   return true;
 }
 
-bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D) {
+bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -123,7 +123,7 @@ bool bwd_layout(int B, int Hq, int Sq, int D, BwdLayout* L) {
   L->off_delta = align256(L->off_dq_acc + rows * D * sizeof(float));
   L->off_lse2 = align256(L->off_delta + rows * sizeof(float));
   L->off_sem = align256(L->off_lse2 + rows * sizeof(float));
-  L->total = align256(L->off_sem + (size_t)B * Hq * (nq > 0 ? nq : 1) * sizeof(int));
+  L->total = align256(L->off_sem + (size_t)B * Hq * (2 * nq > 0 ? 2 * nq : 1) * sizeof(int));
   return true;
 }
 
@@ -224,8 +224,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   const void* do_map = has_q ? dO : k;
   const int bh_map = has_q ? B * Hq : B * Hkv;
   const int sq_map = has_q ? Sq : Sk;
-  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D) || !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) ||
-      !make_tmap_bsd(&tv, v, B * Hkv, Sk, D) || !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D))
+  // q and dO move in 64-row blocks in the backward pass
+  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D, 64) ||
+      !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) || !make_tmap_bsd(&tv, v, B * Hkv, Sk, D) ||
+      !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D, 64))
     return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdArgs a{};
@@ -247,6 +249,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.Sk = Sk;
   a.D = D;
   a.n_qtiles = (Sq + kTile - 1) / kTile;
+  a.n_qblk = (Sq + 63) / 64;
   a.Sq_pad = a.n_qtiles * kTile;
   a.n_ktiles = (Sk + kTile - 1) / kTile;
   a.n_units = B * Hkv * a.n_ktiles;

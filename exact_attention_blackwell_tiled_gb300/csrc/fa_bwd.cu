@@ -3,39 +3,50 @@
 // The pages give no backward mathematics; the kernels compute the textbook
 // gradient of exact attention, recomputing P from the saved log-sum-exp
 // (FlashAttention-4 pages, key contribution #3: tensor-memory accumulators in
-// the backward pass; the dQ reduction through global atomic adds, and the
-// deterministic mode of the Limitations list that serialises those reductions
-// through semaphores).
+// the backward pass and a restructured dQ reduction with fewer global atomic
+// adds; the Limitations list's deterministic mode that serialises the
+// reductions through semaphores).
 //
-//   1. bwd_preprocess  Delta_i = sum_d dO_id O_id, LSE*log2(e) (+inf on padded
-//                      rows), clears the fp32 dQ accumulator, the semaphores and
+//   1. bwd_preprocess  Delta_i = sum_d dO_id O_id and LSE*log2(e) (+inf on padded
+//                      rows); clears the fp32 dQ accumulator, the semaphores and
 //                      the status word.
 //   2. bwd_main        persistent over (batch, kv head, 128-row kv tile j).  K_j
 //                      and V_j stay in shared memory; for every q head of the
-//                      group and every q tile i that can see tile j:
-//                        S^T  = K_j Q_i^T              (TMEM, rows = keys)
-//                        P^T  = 2^(S^T*scale*log2e - LSE2_i)   -> bf16 in TMEM
-//                        dP^T = V_j dO_i^T             (TMEM)
-//                        dS^T = P^T * (dP^T - Delta_i) -> bf16 in TMEM and smem
-//                        dV_j += P^T dO_i,  dK_j += dS^T Q_i   (TMEM accumulators)
-//                        dQ_i  = dS K_j  (TMEM) -> fp32 atomic add into the
-//                                accumulator (deterministic mode: in kv-tile
-//                                order behind a per-(b, h, i) semaphore)
-//                      then dK_j * scale and dV_j are written as bf16.
+//                      group and every 64-row query block i that can see tile j:
+//                        S^T  = K_j Q_i^T                  (TMEM, rows = keys)
+//                        P^T  = 2^(S^T*scale*log2e - LSE2_i) -> bf16 in TMEM
+//                        dP^T = V_j dO_i^T                 (TMEM)
+//                        dS^T = P^T * (dP^T - Delta_i)     -> bf16 in TMEM and smem
+//                        dV_j += P^T dO_i,  dK_j += dS^T Q_i  (TMEM accumulators)
+//                        dQ_i^T = K_j^T dS_i^T             (TMEM, rows = head dim)
+//                      dQ_i^T is staged in shared memory as [query][dim] fp32
+//                      and added to the accumulator with ONE bulk TMA
+//                      reduce-add per block (no per-element atomics); in the
+//                      deterministic mode those reductions run in kv-tile order
+//                      behind a per-(b, h, block) semaphore.  At the end of the
+//                      unit dK_j * scale and dV_j are written as bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
 //
-// bwd_main warp roles (192 threads): warps 0-3 compute P/dS and drain dQ and
-// dK/dV (thread r owns TMEM lane r); warp 4 issues TMA loads; warp 5 owns TMEM
-// and issues every tcgen05.mma from one thread.
-// TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D),
-// dK [256+D,256+2D); dQ: D=64 [384,448), D=128 two 64-column halves in the
-// columns P^T and dS^T leave free, [64,128) and [192,256).
+// bwd_main warp roles (320 threads):
+//   warps 0-3  P^T / dS^T, one key row per thread (TMEM lane);
+//   warps 4-7  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
+//   warp 8     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
+//              block into a 3-stage ring;
+//   warp 9     TMEM owner and single-thread tcgen05.mma issuer.
+// TMEM columns: S^T/P^T double buffer [0,64) [64,128), dP^T/dS^T [128,192),
+// dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
+// MMA issue order per block i: S^T(i+1), dV(i), dK(i), dQ^T(i), dP^T(i+1), so
+// the tensor core works on the next block while the softmax warps finish this
+// one.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
+// block twice; lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
 
 namespace fa {
+
+constexpr int kQB = 64;  // query rows per backward block
 
 // ------------------------------------------------------------------ preprocess
 
@@ -69,7 +80,7 @@ __global__ void bwd_preprocess(const BwdArgs a) {
 #pragma unroll
     for (int e = 0; e < kPer; ++e) dqa[e] = 0.f;
   }
-  const long long nsem = (long long)a.B * a.Hq * a.n_qtiles;
+  const long long nsem = (long long)a.B * a.Hq * a.n_qblk;
   for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < nsem;
        s += (long long)gridDim.x * blockDim.x)
     a.sem[s] = 0;
@@ -79,49 +90,71 @@ __global__ void bwd_preprocess(const BwdArgs a) {
 // ------------------------------------------------------------------ main kernel
 
 template <int D>
-struct BwdLayoutSmem {
+struct BwdSmem {
   static constexpr int kColBlocks = D / 64;
-  static constexpr int kBlockBytes = kTile * 128;
-  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kKVBlockBytes = kTile * 128;           // 128 rows x 64 cols bf16
+  static constexpr int kKVTileBytes = kTile * D * 2;
+  static constexpr int kQBlockBytes = kQB * 128;              // 64 rows x 64 cols bf16
+  static constexpr int kQTileBytes = kQB * D * 2;
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = 2 * kQTileBytes + 1024;  // Q, dO, LSE2 + Delta (padded)
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ0 = kOffV + kTileBytes;  // stage s: Q at kOffQ0 + s*2*kTileBytes,
-                                                     // dO right after it
-  static constexpr int kOffDS = kOffQ0 + 4 * kTileBytes;  // dS^T, 128 keys x 128 queries bf16
-  static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int kOffBar = kOffDS + kDSBytes;
-  static constexpr int kBarKVFull = 0;
-  static constexpr int kBarKVEmpty = 1;
-  static constexpr int kBarQFull = 2;   // 2 stages
-  static constexpr int kBarQEmpty = 4;  // 2 stages
-  static constexpr int kBarSFull = 6;
-  static constexpr int kBarPReady = 7;
-  static constexpr int kBarDSReady = 8;
-  static constexpr int kBarDQFull = 9;
-  static constexpr int kBarDQEmpty = 10;
-  static constexpr int kBarDKVFull = 11;
-  static constexpr int kBarDKVEmpty = 12;
-  static constexpr int kBarDrain = 13;
-  static constexpr int kNumBars = 14;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffV = kOffK + kKVTileBytes;
+  static constexpr int kOffStage = kOffV + kKVTileBytes;
+  static constexpr int kOffDS = kOffStage + kStages * kStageBytes;  // dS^T [key][64 queries]
+  static constexpr int kDSBytes = kTile * kQB * 2;
+  static constexpr int kOffDQ = kOffDS + kDSBytes;  // dQ staging [64 queries][D] fp32
+  static constexpr int kDQBytes = kQB * D * 4;
+  static constexpr int kOffBar = kOffDQ + kDQBytes;
+  static constexpr int kBarKVFull = 0, kBarKVEmpty = 1;
+  static constexpr int kBarQFull = 2;                // kStages
+  static constexpr int kBarQEmpty = 2 + kStages;     // kStages
+  static constexpr int kBarSFull = 2 + 2 * kStages;  // 2
+  static constexpr int kBarPReady = kBarSFull + 2;
+  static constexpr int kBarDPFull = kBarPReady + 1;
+  static constexpr int kBarDSReady = kBarDPFull + 1;
+  static constexpr int kBarDQFull = kBarDSReady + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarDKVFull = kBarDQEmpty + 1;
+  static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
+  static constexpr int kBarDrain = kBarDKVEmpty + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, sem flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  __host__ __device__ static constexpr uint32_t col_dq(int half) {
-    return D == 64 ? 384u : (half == 0 ? 64u : 192u);
-  }
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256,
+                            kColDK = 256 + D;
 };
 
-// q tiles that kv tile j contributes to: [lo, n_qtiles)
-__device__ __forceinline__ int bwd_q_lo(const BwdArgs& a, int j) {
+// first 64-row query block that kv tile j contributes to
+__device__ __forceinline__ int bwd_qblk_lo(const BwdArgs& a, int j) {
   if (!a.causal) return 0;
-  return (j * kTile < a.Sq) ? j : a.n_qtiles;
+  return (j * kTile < a.Sq) ? (j * kTile) / kQB : a.n_qblk;
 }
 
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volatile int* abort) {
   const bool ok = mbar_wait(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// AND of `ok` over the 128 threads of a warpgroup (named barrier `id`); every
+// thread of the group must call it the same number of times.
+__device__ __forceinline__ bool group_all(bool ok, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
 __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
@@ -137,31 +170,87 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+      "r"(w[15])
+      : "memory");
+}
+
+// Iterations (q head of the group x query block) of kv tile j.
+struct BwdUnit {
+  int bhk, j, b, hk, lo, n_blk, n_it;
+};
+
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) {
+  BwdUnit w;
+  w.bhk = u / a.n_ktiles;
+  w.j = u - w.bhk * a.n_ktiles;
+  w.b = w.bhk / a.Hkv;
+  w.hk = w.bhk - w.b * a.Hkv;
+  w.lo = bwd_qblk_lo(a, w.j);
+  w.n_blk = a.n_qblk - w.lo;
+  w.n_it = group * w.n_blk;
+  return w;
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
-  using L = BwdLayoutSmem<D>;
+  using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  volatile int* sem_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8 * i; };
+  auto stage_off = [&](uint32_t it) -> uint32_t {
+    return L::kOffStage + (it % L::kStages) * L::kStageBytes;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarKVFull), 1);
     mbar_init(bar(L::kBarKVEmpty), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
       mbar_init(bar(L::kBarQEmpty + s), 1);
     }
-    mbar_init(bar(L::kBarSFull), 1);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
     mbar_init(bar(L::kBarPReady), 128);
+    mbar_init(bar(L::kBarDPFull), 1);
     mbar_init(bar(L::kBarDSReady), 128);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
@@ -169,13 +258,14 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar(L::kBarDKVEmpty), 128);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
+    *sem_flag = 1;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -187,118 +277,140 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
-        const int bhk = u / a.n_ktiles;
-        const int j = u - bhk * a.n_ktiles;
-        const int b = bhk / a.Hkv, hk = bhk - (bhk / a.Hkv) * a.Hkv;
+        const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVEmpty), (unit & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kTileBytes);
+        mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVTileBytes);
 #pragma unroll
         for (int cb = 0; cb < L::kColBlocks; ++cb) {
-          tma_load_3d(sbase + L::kOffK + cb * L::kBlockBytes, &tm_k, bar(L::kBarKVFull), cb * 64,
-                      j * kTile, bhk);
-          tma_load_3d(sbase + L::kOffV + cb * L::kBlockBytes, &tm_v, bar(L::kBarKVFull), cb * 64,
-                      j * kTile, bhk);
+          tma_load_3d(sbase + L::kOffK + cb * L::kKVBlockBytes, &tm_k, bar(L::kBarKVFull),
+                      cb * 64, w.j * kTile, w.bhk);
+          tma_load_3d(sbase + L::kOffV + cb * L::kKVBlockBytes, &tm_v, bar(L::kBarKVFull),
+                      cb * 64, w.j * kTile, w.bhk);
         }
-        const int lo = bwd_q_lo(a, j);
-        for (int gi = 0; ok && gi < group; ++gi) {
-          const int bh = b * a.Hq + hk * group + gi;
-          for (int i = lo; i < a.n_qtiles; ++i, ++it) {
-            const uint32_t st = it & 1;
-            if (!mbar_wait(bar(L::kBarQEmpty + st), ((it >> 1) & 1) ^ 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar(L::kBarQFull + st), 2 * L::kTileBytes);
-            const uint32_t qdst = sbase + L::kOffQ0 + st * 2 * L::kTileBytes;
-#pragma unroll
-            for (int cb = 0; cb < L::kColBlocks; ++cb) {
-              tma_load_3d(qdst + cb * L::kBlockBytes, &tm_q, bar(L::kBarQFull + st), cb * 64,
-                          i * kTile, bh);
-              tma_load_3d(qdst + L::kTileBytes + cb * L::kBlockBytes, &tm_do,
-                          bar(L::kBarQFull + st), cb * 64, i * kTile, bh);
-            }
+        for (int t = 0; t < w.n_it; ++t, ++it) {
+          const int gi = t / w.n_blk;
+          const int iq = w.lo + (t - gi * w.n_blk);
+          const int bh = w.b * a.Hq + w.hk * group + gi;
+          const uint32_t st = it % L::kStages;
+          if (!mbar_wait(bar(L::kBarQEmpty + st), ((it / L::kStages) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
           }
+          const uint32_t sdst = sbase + stage_off(it);
+          mbar_arrive_expect_tx(bar(L::kBarQFull + st), 2 * L::kQTileBytes + 2 * kQB * 4);
+#pragma unroll
+          for (int cb = 0; cb < L::kColBlocks; ++cb) {
+            tma_load_3d(sdst + cb * L::kQBlockBytes, &tm_q, bar(L::kBarQFull + st), cb * 64,
+                        iq * kQB, bh);
+            tma_load_3d(sdst + L::kQTileBytes + cb * L::kQBlockBytes, &tm_do,
+                        bar(L::kBarQFull + st), cb * 64, iq * kQB, bh);
+          }
+          const size_t voff = (size_t)bh * a.Sq_pad + (size_t)iq * kQB;
+          bulk_load(sdst + 2 * L::kQTileBytes, a.lse2 + voff, kQB * 4, bar(L::kBarQFull + st));
+          bulk_load(sdst + 2 * L::kQTileBytes + kQB * 4, a.delta + voff, kQB * 4,
+                    bar(L::kBarQFull + st));
         }
       }
       if (unit > 0) drain_wait_b(bar(L::kBarKVFull), (unit - 1) & 1);
-      for (uint32_t n = (it > 2 ? it - 2 : 0); n < it; ++n)
-        drain_wait_b(bar(L::kBarQFull + (n & 1)), (n >> 1) & 1);
+      for (uint32_t n = (it > (uint32_t)L::kStages ? it - L::kStages : 0); n < it; ++n)
+        drain_wait_b(bar(L::kBarQFull + n % L::kStages), (n / L::kStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false, false);
-      constexpr uint32_t kIdescAcc = idesc_bf16_f32(kTile, D, false, true);
-      constexpr uint32_t kIdescDQ = idesc_bf16_f32(kTile, 64, true, true);
+      constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kQB, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, false, true);   // dV, dK
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, kQB, true, true);   // dQ^T
+      // K^T as the MN-major A operand of dQ^T: the second 64-row head-dim block
+      // is the second column block of K (D = 128) or, at D = 64, the first again.
+      constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
+      const uint32_t k_base = sbase + L::kOffK, v_base = sbase + L::kOffV;
+      const uint32_t ds_base = sbase + L::kOffDS;
       uint32_t it = 0, unit = 0;
       bool ok = true;
+      auto wait_q = [&](uint32_t i) -> bool {
+        return mbar_wait(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag);
+      };
+      auto issue_s = [&](uint32_t i) {  // S^T(i) = K Q_i^T into buffer i % 2
+        const uint32_t q_base = sbase + stage_off(i);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kColS + (i & 1) * kQB,
+                  sdesc_sw128(k_base + (kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(q_base + (kk >> 2) * L::kQBlockBytes + (kk & 3) * 32, 16, 1024),
+                  kIdS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(L::kBarSFull + (i & 1)));
+      };
+      auto issue_dp = [&](uint32_t i) {  // dP^T(i) = V dO_i^T
+        const uint32_t do_base = sbase + stage_off(i) + L::kQTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kColDP,
+                  sdesc_sw128(v_base + (kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(do_base + (kk >> 2) * L::kQBlockBytes + (kk & 3) * 32, 16, 1024),
+                  kIdS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(L::kBarDPFull));
+      };
       for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
-        const int j = u % a.n_ktiles;
-        const int n_it = group * (a.n_qtiles - bwd_q_lo(a, j));
-        if (unit > 0 && !mbar_wait(bar(L::kBarDKVEmpty), (unit - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+        const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t k_base = sbase + L::kOffK, v_base = sbase + L::kOffV;
-        for (int t = 0; t < n_it; ++t, ++it) {
-          const uint32_t st = it & 1;
-          const uint32_t q_base = sbase + L::kOffQ0 + st * 2 * L::kTileBytes;
-          const uint32_t do_base = q_base + L::kTileBytes;
-          if (!mbar_wait(bar(L::kBarQFull + st), (it >> 1) & 1, abort_flag)) { ok = false; break; }
-          // previous dQ drained (its columns overlap S^T / dP^T when D = 128)
+        // dV / dK accumulators are free once the previous unit's epilogue has read
+        // them; waited right before this unit's first dV MMA
+        auto wait_dkv_free = [&]() -> bool {
+          return unit == 0 || mbar_wait(bar(L::kBarDKVEmpty), (unit - 1) & 1, abort_flag);
+        };
+        if (w.n_it == 0) {
+          if (!wait_dkv_free()) { ok = false; break; }
+        } else {
+          if (!wait_q(it)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(it);
+          issue_dp(it);
+        }
+        for (int t = 0; t < w.n_it; ++t, ++it) {
+          const uint32_t q_base = sbase + stage_off(it);
+          const uint32_t do_base = q_base + L::kQTileBytes;
+          if (t + 1 < w.n_it) {
+            if (!wait_q(it + 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          if (!mbar_wait(bar(L::kBarPReady), it & 1, abort_flag)) { ok = false; break; }
+          if (t == 0 && !wait_dkv_free()) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kQB / 16; ++kk)  // dV += P^T dO  (K = queries)
+            umma_ts(tmem + L::kColDV, tmem + L::kColS + (it & 1) * kQB + kk * 8,
+                    sdesc_sw128(do_base + kk * 16 * 128, L::kQBlockBytes, 1024), kIdAcc,
+                    (t > 0 || kk > 0) ? 1u : 0u);
+          if (!mbar_wait(bar(L::kBarDSReady), it & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kQB / 16; ++kk)  // dK += dS^T Q
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8,
+                    sdesc_sw128(q_base + kk * 16 * 128, L::kQBlockBytes, 1024), kIdAcc,
+                    (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(L::kBarQEmpty + it % L::kStages));
+          // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
+          // previous block has emptied the dQ^T columns
           if (it > 0 && !mbar_wait(bar(L::kBarDQEmpty), (it - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + L::kColS, sdesc_sw128(k_base + off, 16, 1024),
-                    sdesc_sw128(q_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + L::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                    sdesc_sw128(do_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(L::kBarSFull));
-          if (!mbar_wait(bar(L::kBarPReady), it & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)  // dV += P^T dO  (K = queries)
-            umma_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8,
-                    sdesc_sw128(do_base + kk * 16 * 128, L::kBlockBytes, 1024), kIdescAcc,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-          if (!mbar_wait(bar(L::kBarDSReady), it & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dS^T Q
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8,
-                    sdesc_sw128(q_base + kk * 16 * 128, L::kBlockBytes, 1024), kIdescAcc,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-          const uint32_t ds_base = sbase + L::kOffDS;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ = dS K  (K = keys)
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf)
-              umma_ss(tmem + L::col_dq(hf),
-                      sdesc_sw128(ds_base + kk * 16 * 128, L::kBlockBytes, 1024),
-                      sdesc_sw128(k_base + hf * L::kBlockBytes + kk * 16 * 128, L::kBlockBytes,
-                                  1024),
-                      kIdescDQ, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(L::kBarQEmpty + st));
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ss(tmem + L::kColDQ, sdesc_sw128(k_base + kk * 16 * 128, kLboKT, 1024),
+                    sdesc_sw128(ds_base + kk * 16 * 128, 1024, 1024), kIdDQ, kk > 0 ? 1u : 0u);
           umma_commit(bar(L::kBarDQFull));
+          if (t + 1 < w.n_it) issue_dp(it + 1);
         }
         if (!ok) break;
         umma_commit(bar(L::kBarKVEmpty));
@@ -307,163 +419,158 @@ __global__ void __launch_bounds__(192, 1)
       umma_commit(bar(L::kBarDrain));
       drain_wait_b(bar(L::kBarDrain), 0);
     }
-  } else {
-    // ------------------------------------------------------------ P / dS / drains
-    const int r = threadIdx.x;  // key row of the kv tile (and q row for the dQ drain)
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T / dS^T
+    const int r = threadIdx.x;  // key row of the kv tile == TMEM lane
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t it = 0, unit = 0;
+    uint8_t* ds_row = smem + L::kOffDS + r * 128;
+    uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
-      const int bhk = u / a.n_ktiles;
-      const int j = u - bhk * a.n_ktiles;
-      const int b = bhk / a.Hkv, hk = bhk - (bhk / a.Hkv) * a.Hkv;
-      const int kv = j * kTile + r;
-      const int lo = bwd_q_lo(a, j);
-      const int n_qt = a.n_qtiles - lo;
-      const int n_it = group * n_qt;
-      for (int t = 0; t < n_it; ++t, ++it) {
-        const int gi = t / n_qt;
-        const int i = lo + (t - gi * n_qt);
-        const int bh = b * a.Hq + hk * group + gi;
-        const size_t vec_off = (size_t)bh * a.Sq_pad + (size_t)i * kTile;
-        // LSE2 / Delta of the 128 queries: every lane reads the same addresses
-        // (broadcast through L1).
-        const float4* lse4 = reinterpret_cast<const float4*>(a.lse2 + vec_off);
-        const float4* del4 = reinterpret_cast<const float4*>(a.delta + vec_off);
-        if (!warp_wait_b(bar(L::kBarSFull), it & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // ---- P^T row: key kv, queries i*128 + c
-        float p[kTile];
-        const bool row_dead = kv >= a.Sk;
-        const int causal_lim = a.causal ? kv - i * kTile : -1;  // queries c < lim are masked
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColS + c4 * 32, v);
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l = __ldg(lse4 + c4 * 8 + e4);
-            const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = c4 * 32 + e4 * 4 + e;
-              float x = ex2_mufu(u2f(v[e4 * 4 + e]) * a.scale_log2 - lv[e]);
-              if (row_dead || c < causal_lim) x = 0.f;
-              p[c] = x;
-            }
-          }
+    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+      const BwdUnit w = bwd_unit(a, u, group);
+      const int kv = w.j * kTile + r;
+      const bool row_dead = kv >= a.Sk;
+      for (int t = 0; t < w.n_it; ++t, ++it) {
+        const int gi = t / w.n_blk;
+        const int iq = w.lo + (t - gi * w.n_blk);
+        const float* s_lse2 =
+            reinterpret_cast<const float*>(smem + stage_off(it) + 2 * L::kQTileBytes);
+        const float* s_delta = s_lse2 + kQB;
+        if (!warp_wait_b(bar(L::kBarQFull + it % L::kStages), (it / L::kStages) & 1,
+                         abort_flag) ||
+            !warp_wait_b(bar(L::kBarSFull + (it & 1)), (it >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        // queries c with iq*64 + c < kv are masked (causal)
+        const int causal_lim = a.causal ? kv - iq * kQB : -1;
+        float p[kQB];
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t w[32];
+          uint32_t v[32];
+          tmem_ld32(t_row + L::kColS + (it & 1) * kQB + c2 * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(p[c2 * 64 + 2 * e], p[c2 * 64 + 2 * e + 1]);
-          tmem_st32(t_row + L::kColS + c2 * 32, w);
+          for (int e = 0; e < 32; ++e) {
+            const int c = c2 * 32 + e;
+            const float x = ex2_mufu(u2f(v[e]) * a.scale_log2 - s_lse2[c]);
+            p[c] = (row_dead || c < causal_lim) ? 0.f : x;
+          }
+        }
+        {
+          uint32_t wbuf[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wbuf[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+          tmem_st32(t_row + L::kColS + (it & 1) * kQB, wbuf);
         }
         tc_fence_before();
         mbar_arrive(bar(L::kBarPReady));
-        // ---- dS^T row = P^T * (dP^T - Delta); written packed over the dP^T
-        // columns already read, and to shared memory for the dQ MMA
-        uint8_t* ds_row = smem + L::kOffDS + r * 128;
+        if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t v[32];
-          tmem_ld32(t_row + L::kColDP + c4 * 32, v);
-          uint32_t w[16];
+          tmem_ld32(t_row + L::kColDP + c2 * 32, v);
+          uint32_t wbuf[16];
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 dl = __ldg(del4 + c4 * 8 + e4);
-            const int c = c4 * 32 + e4 * 4;
-            const float d0 = p[c] * (u2f(v[e4 * 4]) - dl.x);
-            const float d1 = p[c + 1] * (u2f(v[e4 * 4 + 1]) - dl.y);
-            const float d2 = p[c + 2] * (u2f(v[e4 * 4 + 2]) - dl.z);
-            const float d3 = p[c + 3] * (u2f(v[e4 * 4 + 3]) - dl.w);
-            w[e4 * 2] = pack_bf16x2(d0, d1);
-            w[e4 * 2 + 1] = pack_bf16x2(d2, d3);
+          for (int e = 0; e < 16; ++e) {
+            const int c = c2 * 32 + 2 * e;
+            const float d0 = p[c] * (u2f(v[2 * e]) - s_delta[c]);
+            const float d1 = p[c + 1] * (u2f(v[2 * e + 1]) - s_delta[c + 1]);
+            wbuf[e] = pack_bf16x2(d0, d1);
           }
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-              "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
-                  t_row + L::kColDP + c4 * 16),
-              "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-              "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
-              "r"(w[14]), "r"(w[15])
-              : "memory");
-          // shared memory, 128-byte swizzle: [query block][key row][64 queries]
+          // packed over the dP^T columns this thread has already read
+          tmem_st16(t_row + L::kColDP + c2 * 16, wbuf);
+          // shared memory, 128-byte swizzle: [key row][64 queries]
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
-            const int qcol = c4 * 32 + ch * 8;  // first query of this 16-byte chunk
-            const int blk = qcol >> 6;
-            const int chunk = (qcol & 63) >> 3;
-            uint4* dst = reinterpret_cast<uint4*>(ds_row + blk * L::kBlockBytes +
-                                                  ((chunk ^ (r & 7)) << 4));
-            *dst = make_uint4(w[ch * 4], w[ch * 4 + 1], w[ch * 4 + 2], w[ch * 4 + 3]);
+            const int chunk = c2 * 4 + ch;  // 16-byte chunk = 8 queries
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                make_uint4(wbuf[ch * 4], wbuf[ch * 4 + 1], wbuf[ch * 4 + 2], wbuf[ch * 4 + 3]);
           }
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(L::kBarDSReady));
-        // ---- dQ drain: thread r now owns query row i*128 + r
-        if (!warp_wait_b(bar(L::kBarDQFull), it & 1, abort_flag)) { ok = false; break; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+    const int r = threadIdx.x - 128;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
+    const int wq = warp - 4;
+    const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
+    float* stage_dq = reinterpret_cast<float*>(smem + L::kOffDQ);
+    uint32_t it = 0, unit = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
+      const BwdUnit w = bwd_unit(a, u, group);
+      for (int t = 0; t < w.n_it; ++t, ++it) {
+        const int gi = t / w.n_blk;
+        const int iq = w.lo + (t - gi * w.n_blk);
+        const int bh = w.b * a.Hq + w.hk * group + gi;
+        ok = group_all(warp_wait_b(bar(L::kBarDQFull), it & 1, abort_flag), 2);
+        if (!ok) break;
         tc_fence_after();
-        int* sem = a.sem + (size_t)bh * a.n_qtiles + i;
-        if (a.deterministic) {
-          // Each of the 4 warps of kv tile j adds its 32 rows once tile j-1's
-          // four warps have finished: the semaphore counts warps, target 4*j.
+        // the previous block's bulk reduce must have finished reading the staging tile
+        if (r == 0) bulk_wait_read();
+        group_sync(2);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t v[32];
+          tmem_ld32(t_row + L::kColDQ + c2 * 32, v);
+          if (r < D) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) stage_dq[(c2 * 32 + e) * D + r] = u2f(v[e]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDQEmpty));
+        fence_proxy_async_smem();
+        group_sync(2);
+        if (r == 0) {
+          float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D;
           int good = 1;
-          if (lane == 0) {
+          if (a.deterministic) {
+            // kv tiles add their part of block iq in ascending order j
+            int* sem = a.sem + (size_t)bh * a.n_qblk + iq;
             const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(sem) != 4 * j) {
+            while (ld_acquire(sem) != w.j) {
               if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
                 *abort_flag = 1;
                 good = 0;
                 break;
               }
             }
-          }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          __syncwarp();
-          if (!good) ok = false;
-        }
-        if (ok) {
-          float* dst = a.dq_acc + (vec_off + r) * D;
-#pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              uint32_t v[32];
-              tmem_ld32(t_row + L::col_dq(hf) + c2 * 32, v);
-              float4* d4 = reinterpret_cast<float4*>(dst + hf * 64 + c2 * 32);
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                atomicAdd(d4 + e, make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]), u2f(v[4 * e + 2]),
-                                              u2f(v[4 * e + 3])));
+            if (good) {
+              bulk_reduce_add_f32(dst, smem_u32(stage_dq), kQB * D * 4);
+              bulk_wait_all();
+              __threadfence();
+              atomicAdd(sem, 1);
             }
+          } else {
+            bulk_reduce_add_f32(dst, smem_u32(stage_dq), kQB * D * 4);
           }
-          if (a.deterministic) {
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) atomicAdd(sem, 1);
-          }
+          *sem_flag = good;
         }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarDQEmpty));
-        if (!ok) break;
+        group_sync(2);
+        if (!*sem_flag) { ok = false; break; }
       }
       if (!ok) break;
       // ---- dK, dV epilogue for key row kv
-      if (!warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag)) { ok = false; break; }
+      ok = group_all(warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag), 2);
+      if (!ok) break;
       tc_fence_after();
+      const int kv = w.j * kTile + r;
       const bool row_ok = kv < a.Sk;
-      const size_t out_off = ((size_t)bhk * a.Sk + (row_ok ? kv : 0)) * D;
+      const size_t out_off = ((size_t)w.bhk * a.Sk + (row_ok ? kv : 0)) * D;
       __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(a.dk) + out_off;
       __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(a.dv) + out_off;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t vk[32], vv[32];
-        __syncwarp();  // reconverge after the per-row stores before the warp-wide loads
-        if (n_it > 0) {
+        __syncwarp();
+        if (w.n_it > 0) {
           tmem_ld32(t_row + L::kColDK + c * 32, vk);
           tmem_ld32(t_row + L::kColDV + c * 32, vv);
         } else {
@@ -489,11 +596,13 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarDKVEmpty));
     }
+    // outstanding bulk reductions must finish before the kernel ends
+    if (r == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -527,7 +636,7 @@ __global__ void bwd_dq_convert(const BwdArgs a) {
 template <int D>
 static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayoutSmem<D>;
+  using L = BwdSmem<D>;
   int dev;
   DeviceInfo info;
   if (!current_device(&dev, &info)) return FA_ERR_CUDA;
@@ -556,7 +665,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(192);
+      cfg.blockDim = dim3(320);
       cfg.dynamicSmemBytes = L::kAllocBytes;
       cfg.stream = stream;
       cudaLaunchAttribute attr[1];
@@ -567,7 +676,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       if (cudaLaunchKernelEx(&cfg, bwd_main<D>, tq, tk, tv, tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
-      bwd_main<D><<<grid, 192, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
+      bwd_main<D><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
     }
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     record_timing(true, stream);

@@ -24,9 +24,10 @@ struct DeviceInfo {
 // Cached attributes of the current device; false if no device is usable.
 bool current_device(int* dev, DeviceInfo* info);
 
-// Encodes a 3-D tensor map over a [BH, S, D] bf16 tensor with 128-row x
+// Encodes a 3-D tensor map over a [BH, S, D] bf16 tensor with box_rows-row x
 // 64-column boxes and the 128-byte swizzle.  Returns false on failure.
-bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D);
+bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D,
+                   int box_rows = kTile);
 
 struct FwdArgs {
   void* o;
@@ -55,7 +56,7 @@ struct BwdArgs {
   float* dq_acc;   // [B, Hq, Sq_pad, D]
   float* delta;    // [B, Hq, Sq_pad]
   float* lse2;     // [B, Hq, Sq_pad]
-  int* sem;        // [B, Hq, n_qtiles]
+  int* sem;        // [B, Hq, n_qblk]
   int* status;     // [1]
   int B, Hq, Hkv, Sq, Sk, D;
   int Sq_pad;
@@ -63,8 +64,9 @@ struct BwdArgs {
   int deterministic;
   float scale;
   float scale_log2;
-  int n_qtiles;
-  int n_ktiles;
+  int n_qtiles;  // 128-row tiles of Sq
+  int n_qblk;    // 64-row query blocks of Sq (the backward's q step)
+  int n_ktiles;  // 128-row kv tiles of Sk
   int n_units;
 };
 

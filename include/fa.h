@@ -79,8 +79,8 @@ int fa_fwd_status(fa_stream_t stream);
  * Bytes of device workspace fa_bwd needs for these sizes (0 on bad sizes).  The
  * workspace holds an fp32 dQ accumulator [B, Hq, ceil(Sq/128)*128, D], the
  * per-row dot products D_i = dO_i . O_i and LSE*log2(e) (fp32 [B, Hq, padded
- * Sq]), the deterministic mode's per-(b, h, q-tile) semaphores and a status
- * word.  It needs no initialisation: fa_bwd clears what it uses.
+ * Sq]), the deterministic mode's per-(b, h, 64-row query block) semaphores and
+ * a status word.  It needs no initialisation: fa_bwd clears what it uses.
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
 

@@ -126,3 +126,13 @@ def test_gqa_spike_sampled():
                                         (16384, 64, True), (32768, 128, False)])
 def test_sweep_sampled(S, D, causal):
     _sampled(synth.sweep(S, D, causal), 16 if S >= 16384 else 48, 0)
+
+
+def test_timing_events_bracket_the_kernel():
+    w = synth.Workload("t", 1, 4, 4, 1024, 1024, 128, False, 3)
+    q, k, v = (t.to(DEV) for t in synth.make_inputs(w))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.set_timing_events(e0, e1)
+    fa.fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0
