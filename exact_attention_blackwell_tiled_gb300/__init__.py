@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 
 #: every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
-           "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events")
+           "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
+           "fa_bwd_noalloc")
 
 _LIB = None
 
@@ -57,6 +58,9 @@ def _bind(lib):
     lib.fa_last_launch_count.restype = i
     lib.fa_set_timing_events.argtypes = [vp, vp]
     lib.fa_set_timing_events.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i,
+                                   vp]
+    lib.fa_bwd_noalloc.restype = i
     return lib
 
 

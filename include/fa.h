@@ -134,6 +134,33 @@ int fa_last_launch_count(void);
  */
 int fa_set_timing_events(void* start_event, void* stop_event);
 
+/*
+ * Backward pass for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this exists for code that is not allowed to call cudaMalloc
+ * or to own a workspace buffer (for example code running inside another
+ * framework's allocator or memory pool, or a plugin limited to the buffers it
+ * is handed).  It computes exactly what fa_bwd computes, with the same
+ * arguments minus the workspace: the workspace is a fixed 32 MiB scratch array
+ * compiled into this library, which every GPU that loads the library keeps
+ * until the process exits.  No call allocates or frees memory.
+ *   - Sizes whose workspace (fa_bwd_workspace_bytes) exceeds 32 MiB are
+ *     rejected with FA_ERR_WORKSPACE (about 64,000 query rows B*Hq*Sq at
+ *     D = 128, about 127,000 at D = 64); invalid sizes return
+ *     FA_ERR_INVALID_ARG.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one scratch array and it keeps the last call's
+ *     contents; each call clears what it needs cleared.  Calls that overlap on
+ *     the GPU (different streams, or different host threads without ordering)
+ *     race on it and produce wrong gradients: serialise them.
+ *   - Device-side timeouts are recorded in the scratch and cannot be read back
+ *     through fa_bwd_status.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+                   int Sk, int D, int causal, float scale, int deterministic, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
