@@ -180,7 +180,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_qtiles = (Sq + kTile - 1) / kTile;
-  a.n_units = B * Hq * a.n_qtiles;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  a.n_units = B * Hq * a.n_pairs;
   return launch_fwd(tq, tk, tv, a, D, static_cast<cudaStream_t>(stream));
 }
 

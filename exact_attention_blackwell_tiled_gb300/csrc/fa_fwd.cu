@@ -1,27 +1,32 @@
 // fa_fwd.cu -- forward attention kernel for sm_103a.
 //
-// One persistent CTA per SM walks a list of (batch*head, 128-row Q tile) work
-// units.  For each unit it streams the 128-row K/V tiles of the matching kv head
-// and keeps the online-softmax state of its 128 query rows (FlashAttention-4
-// pages: the three per-tile phases GEMM 1 -> softmax -> GEMM 2, the pipeline
-// "Softmax(S_k) || GEMM 2(P_k V_k) || GEMM 1(Q K_{k+1}^T)", 128x128 tiles,
-// accumulators in tensor memory, conditional rescale with threshold
+// One persistent CTA per SM walks a list of work units.  A unit is a PAIR of
+// 128-row query tiles of one (batch, head) -- 256 query rows -- that stream the
+// same 128-row K/V tiles of the matching kv head (FlashAttention-4 pages: the
+// three per-tile phases GEMM 1 -> softmax -> GEMM 2; the pipeline
+// "Softmax(S_k) || GEMM 2(P_k V_k) || GEMM 1(Q K_{k+1}^T)"; 128x128 tiles with
+// accumulators in tensor memory; conditional rescale with threshold
 // log2(256) = 8.0).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread r owns query row r (= TMEM lane r).  Reads S from
+// Warp roles (320 threads):
+//   warps 0-3  softmax of query tile 0 of the pair, warps 4-7 of tile 1: thread r
+//              of the group owns query row r (= TMEM lane r).  It reads S from
 //              TMEM, masks, updates the running max / sum, writes P (bf16) back
-//              into TMEM over the S columns, rescales O in TMEM when the running
-//              max moved by more than 8 (log2 units), and writes O / LSE at the
-//              end of the unit.
-//   warp 4     TMA producer: Q tile per unit into a 2-stage ring, K and V tiles
-//              into a shared ring in the order the MMA issuer consumes them.
-//   warp 5     TMEM allocator and single-thread tcgen05.mma issuer:
-//              S[g%2] = Q K_g^T (SS MMA), then O += P_{g-1} V_{g-1} (TS MMA,
-//              P read from TMEM), so GEMM 1 of tile g overlaps the softmax of
-//              tile g-1 and GEMM 2 of tile g-1 overlaps the softmax of tile g.
+//              over the S columns, rescales its O row in TMEM when the running
+//              max moved by more than 8 (log2 units), and writes O and the LSE
+//              at the end of the unit.
+//   warp 8     TMA producer: both Q tiles of a unit into a 2-stage ring, then
+//              K_0, V_0, K_1, V_1, ... into a shared ring, the order the MMA
+//              issuer first uses them.
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer.  Per kv tile
+//              j it issues, for tile 0 then tile 1:
+//                O_t += P_t(j-1) V_{j-1}   (TS MMA, P read from TMEM)
+//                S_t  = Q_t K_j^T          (SS MMA)
+//              so while the softmax warps of one tile work, the tensor core
+//              runs the other tile's two GEMMs ("ping-pong").
 //
-// TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256, 256+D).
+// TMEM columns: S/P of tile 0 [0,128), of tile 1 [128,256); O of tile 0
+// [256, 256+D), of tile 1 [256+D, 256+2D).
 // Scores are handled in base 2: t = s * scale * log2(e), P = 2^(t - m).
 #include <cuda_bf16.h>
 
@@ -38,20 +43,24 @@ struct FwdLayout {
   static constexpr int kColBlocks = D / 64;         // 64-element (128-byte) column blocks
   static constexpr int kBlockBytes = kTile * 128;   // one 128-row x 64-col block
   static constexpr int kTileBytes = kTile * D * 2;  // a Q, K or V tile
-  static constexpr int kQStages = 2;
-  static constexpr int kKVStages = (D == 128) ? 4 : 8;
+  // Each Q stage holds both Q tiles.  At D = 128 one Q stage buys two more K/V
+  // stages: the K/V ring must hold V_{j-1} and K_j in use plus enough tiles in
+  // flight to hide the TMA latency, while a single Q stage only delays the next
+  // unit's first GEMM 1 by the part of one Q load its trailing GEMM 2s don't cover.
+  static constexpr int kQStages = (D == 128) ? 1 : 2;
+  static constexpr int kKVStages = (D == 128) ? 5 : 6;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffKV = kOffQ + kQStages * 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kKVStages * kTileBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarQEmpty = kBarQFull + kQStages;
   static constexpr int kBarKVFull = kBarQEmpty + kQStages;
   static constexpr int kBarKVEmpty = kBarKVFull + kKVStages;
-  static constexpr int kBarSFull = kBarKVEmpty + kKVStages;  // 2
-  static constexpr int kBarPFull = kBarSFull + 2;            // 2
-  static constexpr int kBarO = kBarPFull + 2;                // GEMM 2 completions
-  static constexpr int kBarOFree = kBarO + 1;                // epilogue done with O
-  static constexpr int kBarDrain = kBarOFree + 1;
+  static constexpr int kBarSFull = kBarKVEmpty + kKVStages;  // per tile
+  static constexpr int kBarPFull = kBarSFull + 2;            // per tile
+  static constexpr int kBarOFinal = kBarPFull + 2;           // per tile: last GEMM 2 done
+  static constexpr int kBarOFree = kBarOFinal + 2;           // per tile: epilogue done with O
+  static constexpr int kBarDrain = kBarOFree + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM base slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
@@ -78,18 +87,20 @@ __device__ __forceinline__ UnitRange cta_units(const FwdArgs& a) {
   return r;
 }
 
-// Unit u -> (flat batch*head index, q tile).  Units are head-major so that the
-// CTAs running at the same time share the K/V of few heads in L2.  Causal
-// units alternate longest / shortest inside a head so contiguous chunks carry
-// near-equal work.
-__device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& qt) {
-  const int nq = a.n_qtiles;
-  bh = u / nq;
-  const int r = u - bh * nq;
-  qt = a.causal ? ((r & 1) ? (r >> 1) : (nq - 1 - (r >> 1))) : r;
+// Unit u -> (flat batch*head index, tile pair p: query tiles 2p and 2p+1).
+// Units are head-major so that the CTAs running at the same time share the K/V
+// of few heads in L2.  Causal pairs alternate longest / shortest inside a head
+// so contiguous chunks carry near-equal work.
+__device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& pair) {
+  const int np = a.n_pairs;
+  bh = u / np;
+  const int r = u - bh * np;
+  pair = a.causal ? ((r & 1) ? (r >> 1) : (np - 1 - (r >> 1))) : r;
 }
 
-__device__ __forceinline__ int unit_kv_tiles(const FwdArgs& a, int qt) {
+// kv tiles query tile qt needs (0 when the tile lies past Sq)
+__device__ __forceinline__ int tile_kv_count(const FwdArgs& a, int qt) {
+  if (qt * kTile >= a.Sq) return 0;
   int kv_len = a.Sk;
   if (a.causal) kv_len = min(a.Sk, min(a.Sq, (qt + 1) * kTile));
   return (kv_len + kTile - 1) / kTile;
@@ -111,7 +122,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = FwdLayout<D>;
@@ -134,21 +145,21 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(L::kBarKVFull + s), 1);
       mbar_init(bar(L::kBarKVEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kBarSFull + s), 1);
-      mbar_init(bar(L::kBarPFull + s), 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kBarSFull + t), 1);
+      mbar_init(bar(L::kBarPFull + t), 128);
+      mbar_init(bar(L::kBarOFinal + t), 1);
+      mbar_init(bar(L::kBarOFree + t), 128);
     }
-    mbar_init(bar(L::kBarO), 1);
-    mbar_init(bar(L::kBarOFree), 128);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -159,14 +170,11 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
   const UnitRange ur = cta_units(a);
   const int group = a.Hq / a.Hkv;
-
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
-      bool have_v = false;
-      int v_bhk = 0, v_j = 0;
       auto load_kv = [&](const CUtensorMap* tm, int bhk, int j) -> bool {
         const uint32_t st = kv_it % L::kKVStages;
         if (!mbar_wait(bar(L::kBarKVEmpty + st), ((kv_it / L::kKVStages) & 1) ^ 1, abort_flag))
@@ -181,206 +189,276 @@ __global__ void __launch_bounds__(192, 1)
         return true;
       };
       for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
-        int bh, qt;
-        unit_coords(a, u, bh, qt);
-        const int b = bh / a.Hq, h = bh - (bh / a.Hq) * a.Hq;
+        int bh, pair;
+        unit_coords(a, u, bh, pair);
+        const int b = bh / a.Hq, h = bh - b * a.Hq;
         const int bhk = b * a.Hkv + h / group;
-        const int n_kv = unit_kv_tiles(a, qt);
+        const int n0 = tile_kv_count(a, 2 * pair), n1 = tile_kv_count(a, 2 * pair + 1);
+        const int nmax = n0 > n1 ? n0 : n1;
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQEmpty + qs), ((q_it / L::kQStages) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(L::kBarQFull + qs), L::kTileBytes);
+        mbar_arrive_expect_tx(bar(L::kBarQFull + qs), 2 * L::kTileBytes);
+        const uint32_t qdst = sbase + L::kOffQ + qs * 2 * L::kTileBytes;
 #pragma unroll
-        for (int cb = 0; cb < L::kColBlocks; ++cb)
-          tma_load_3d(sbase + L::kOffQ + qs * L::kTileBytes + cb * L::kBlockBytes, &tm_q,
-                      bar(L::kBarQFull + qs), cb * 64, qt * kTile, bh);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int cb = 0; cb < L::kColBlocks; ++cb)
+            tma_load_3d(qdst + t * L::kTileBytes + cb * L::kBlockBytes, &tm_q,
+                        bar(L::kBarQFull + qs), cb * 64, (2 * pair + t) * kTile, bh);
         ++q_it;
-        for (int j = 0; j < n_kv; ++j) {
-          if (!load_kv(&tm_k, bhk, j)) { ok = false; break; }
-          if (have_v && !load_kv(&tm_v, v_bhk, v_j)) { ok = false; break; }
-          have_v = true;
-          v_bhk = bhk;
-          v_j = j;
+        for (int j = 0; j < nmax; ++j) {
+          if (!load_kv(&tm_k, bhk, j) || !load_kv(&tm_v, bhk, j)) { ok = false; break; }
         }
       }
-      if (ok && have_v) load_kv(&tm_v, v_bhk, v_j);
       // Let every issued copy land before the CTA can exit.
       for (uint32_t n = (kv_it > (uint32_t)L::kKVStages ? kv_it - L::kKVStages : 0); n < kv_it; ++n)
         drain_wait(bar(L::kBarKVFull + n % L::kKVStages), (n / L::kKVStages) & 1);
       for (uint32_t n = (q_it > (uint32_t)L::kQStages ? q_it - L::kQStages : 0); n < q_it; ++n)
         drain_wait(bar(L::kBarQFull + n % L::kQStages), (n / L::kQStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTile, D, false, true);
-      uint32_t kv_it = 0, q_it = 0, g = 0, tile = 0;
+      uint32_t kv_it = 0, q_it = 0;
+      uint32_t p_seen[2] = {0u, 0u};  // P-ready phases consumed, per tile
+      uint32_t units_t[2] = {0u, 0u};  // units with work, per tile (O-free phases)
       bool ok = true;
-      bool have_prev = false, prev_first = false;
-      uint32_t prev_g = 0, prev_tile = 0;
-      auto gemm2 = [&](uint32_t pg, bool first, uint32_t ptile) -> bool {
-        const uint32_t sb = pg & 1;
-        if (!mbar_wait(bar(L::kBarPFull + sb), (pg >> 1) & 1, abort_flag)) return false;
-        if (first && ptile > 0 && !mbar_wait(bar(L::kBarOFree), (ptile - 1) & 1, abort_flag))
-          return false;
-        const uint32_t st = kv_it % L::kKVStages;
-        if (!mbar_wait(bar(L::kBarKVFull + st), (kv_it / L::kKVStages) & 1, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t v_base = sbase + L::kOffKV + st * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // V as the MN-major B operand: 16 kv rows per step; 64-column blocks
-          // of V are kBlockBytes apart.
-          const uint64_t bdesc = sdesc_sw128(v_base + kk * 16 * 128, L::kBlockBytes, 1024);
-          umma_ts(tmem + L::kColO, tmem + sb * 128 + kk * 8, bdesc, kIdescO,
-                  (kk > 0 || !first) ? 1u : 0u);
-        }
-        umma_commit(bar(L::kBarKVEmpty + st));
-        ++kv_it;
-        umma_commit(bar(L::kBarO));
-        return true;
-      };
       for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
-        int bh, qt;
-        unit_coords(a, u, bh, qt);
-        const int n_kv = unit_kv_tiles(a, qt);
+        int bh, pair;
+        unit_coords(a, u, bh, pair);
+        const int n[2] = {tile_kv_count(a, 2 * pair), tile_kv_count(a, 2 * pair + 1)};
+        const int nmax = n[0] > n[1] ? n[0] : n[1];
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQFull + qs), (q_it / L::kQStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t q_base = sbase + L::kOffQ + qs * L::kTileBytes;
-        for (int j = 0; j < n_kv; ++j) {
-          const uint32_t st = kv_it % L::kKVStages;
-          if (!mbar_wait(bar(L::kBarKVFull + st), (kv_it / L::kKVStages) & 1, abort_flag)) {
+        const uint32_t q_base = sbase + L::kOffQ + qs * 2 * L::kTileBytes;
+        const uint32_t base_it = kv_it;  // ring position of K_0; V_j sits right after K_j
+        for (int j = 0; ok && j <= nmax; ++j) {
+          const bool need_v = j >= 1;
+          const bool need_k = j < nmax;
+          const uint32_t v_pos = base_it + 2 * (j - 1) + 1, k_pos = base_it + 2 * j;
+          const uint32_t v_st = v_pos % L::kKVStages, k_st = k_pos % L::kKVStages;
+          if (need_v && !mbar_wait(bar(L::kBarKVFull + v_st), (v_pos / L::kKVStages) & 1,
+                                   abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (need_k && !mbar_wait(bar(L::kBarKVFull + k_st), (k_pos / L::kKVStages) & 1,
+                                   abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t k_base = sbase + L::kOffKV + st * L::kTileBytes;
-          const uint32_t sb = g & 1;
+          const uint32_t v_base = sbase + L::kOffKV + v_st * L::kTileBytes;
+          const uint32_t k_base = sbase + L::kOffKV + k_st * L::kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // Q and K as K-major operands: 16 head-dim columns per step.
-            const uint32_t off = (kk >> 2) * L::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
-                    sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          for (int t = 0; t < 2; ++t) {
+            if (j >= 1 && j <= n[t]) {
+              // GEMM 2: O_t += P_t(j-1) V_{j-1}
+              if (!mbar_wait(bar(L::kBarPFull + t), p_seen[t] & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              ++p_seen[t];
+              if (j == 1 && units_t[t] > 0 &&
+                  !mbar_wait(bar(L::kBarOFree + t), (units_t[t] - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                umma_ts(tmem + L::kColO + t * D, tmem + t * kTile + kk * 8,
+                        sdesc_sw128(v_base + kk * 16 * 128, L::kBlockBytes, 1024), kIdescO,
+                        (j > 1 || kk > 0) ? 1u : 0u);
+              if (j == n[t]) umma_commit(bar(L::kBarOFinal + t));
+            }
+            if (j < n[t]) {
+              // GEMM 1: S_t = Q_t K_j^T
+              const uint32_t qb = q_base + t * L::kTileBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * L::kBlockBytes + (kk & 3) * 32;
+                umma_ss(tmem + t * kTile, sdesc_sw128(qb + off, 16, 1024),
+                        sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(L::kBarSFull + t));
+            }
           }
-          umma_commit(bar(L::kBarKVEmpty + st));
-          ++kv_it;
-          umma_commit(bar(L::kBarSFull + sb));
-          if (j == n_kv - 1) umma_commit(bar(L::kBarQEmpty + qs));
-          if (have_prev && !gemm2(prev_g, prev_first, prev_tile)) {
-            ok = false;
-            break;
-          }
-          have_prev = true;
-          prev_first = (j == 0);
-          prev_g = g;
-          prev_tile = tile;
-          ++g;
+          if (!ok) break;
+          // stages are released in ring order: V_{j-1} then K_j
+          if (need_v) umma_commit(bar(L::kBarKVEmpty + v_st));
+          if (need_k) umma_commit(bar(L::kBarKVEmpty + k_st));
+          // the Q stage is free once the unit's last GEMM 1 has run
+          if (j == nmax - 1) umma_commit(bar(L::kBarQEmpty + qs));
         }
+        if (!ok) break;
+        kv_it = base_it + 2 * nmax;
         ++q_it;
-        ++tile;
+        for (int t = 0; t < 2; ++t)
+          if (n[t] >= 1) ++units_t[t];
       }
-      if (ok && have_prev) gemm2(prev_g, prev_first, prev_tile);
       // Every issued MMA must complete before TMEM is released.
       umma_commit(bar(L::kBarDrain));
       drain_wait(bar(L::kBarDrain), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int row = threadIdx.x;  // query row inside the tile == TMEM lane
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t g = 0, o_seen = 0;
+    const int t = warp >> 2;           // query tile of the pair this group serves
+    const int r = threadIdx.x & 127;   // query row inside the tile == TMEM lane
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t col_s = t * kTile, col_o = L::kColO + t * D;
+    uint32_t g = 0, nu = 0;  // S-full phases and units consumed by this group
     bool ok = true;
     for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
-      int bh, qt;
-      unit_coords(a, u, bh, qt);
-      const int n_kv = unit_kv_tiles(a, qt);
-      const int q_row = qt * kTile + row;
+      int bh, pair;
+      unit_coords(a, u, bh, pair);
+      const int qt = 2 * pair + t;
+      const int n_kv = tile_kv_count(a, qt);
+      if (n_kv == 0) continue;
+      const int q_row = qt * kTile + r;
       const int lim = a.causal ? min(a.Sk, q_row + 1) : a.Sk;  // keys [0, lim) visible
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_kv; ++j) {
-        const uint32_t sb = g & 1;
-        if (!warp_wait(bar(L::kBarSFull + sb), (g >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(L::kBarSFull + t), g & 1, abort_flag)) { ok = false; break; }
+        ++g;
         tc_fence_after();
-        float t[kTile];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_row + sb * 128 + c * 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) t[c * 32 + i] = u2f(r[i]) * a.scale_log2;
-        }
         const int kv0 = j * kTile;
-        if (kv0 + kTile > lim) {
-#pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (kv0 + c >= lim) t[c] = -INFINITY;
-        }
-        float tmax = t[0];
-#pragma unroll
-        for (int c = 1; c < kTile; ++c) tmax = fmaxf(tmax, t[c]);
-        // Conditional rescale: keep a stale running max unless the new max
-        // exceeds it by more than 8 (P then stays <= 2^8).
+        const bool masked_tile = kv0 + kTile > lim;
+        const float c = a.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
-        if (j == 0) {
-          m_run = tmax;
-        } else if (tmax > m_run + 8.0f) {
-          alpha = ex2_mufu(m_run - tmax);
-          m_run = tmax;
-          rescale = true;
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        uint32_t p[kTile / 2];
-        float sum = 0.f;
+        float2 sum2 = make_float2(0.f, 0.f);
+        // Conditional rescale: keep a stale running max unless the new max
+        // exceeds it by more than 8 (P then stays <= 2^8).
+        auto update_max = [&](float tmax) {
+          if (j == 0) {
+            m_run = tmax;
+          } else if (tmax > m_run + 8.0f) {
+            alpha = ex2_mufu(m_run - tmax);
+            m_run = tmax;
+            rescale = true;
+          }
+        };
+        if (c > 0.f) {
+          // Common case.  Pass 1: the whole score row in one TMEM round trip,
+          // reduced to its max (masked columns skipped).
+          float mraw = -INFINITY;
+          {
+            uint32_t v[kTile];
+            tmem_ld128(t_row + col_s, v);
+            if (masked_tile) {
 #pragma unroll
-        for (int c = 0; c < kTile / 2; ++c) {
-          const float p0 = ex2_mufu(t[2 * c] - m_use);
-          const float p1 = ex2_mufu(t[2 * c + 1] - m_use);
-          sum += p0 + p1;
-          p[c] = pack_bf16x2(p0, p1);
-        }
-        l_run = l_run * alpha + sum;
-        // GEMM 2 of the previous tile must be done before O is touched or the
-        // next P is published (keeps one GEMM 2 phase outstanding at most).
-        while (o_seen < g) {
-          if (!warp_wait(bar(L::kBarO), o_seen & 1, abort_flag)) { ok = false; break; }
-          ++o_seen;
-        }
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+              for (int i = 0; i < kTile; ++i)
+                if (kv0 + i >= lim) v[i] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int i = 0; i < kTile; i += 2) mraw = fmax3(mraw, u2f(v[i]), u2f(v[i + 1]));
+          }
+          update_max(mraw == -INFINITY ? -INFINITY : mraw * c);
+          const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+          // Pass 2, one half-row (64 scores) per round trip: P = 2^(s*c - m)
+          // with one packed FMA per two scores; masked columns are -inf and
+          // give P = 0.  Each half of P (32 packed columns) is stored over S
+          // columns already read.
+          const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t w0[32], w1[32], pk[32];
+            __syncwarp();
+            tmem_ld32(t_row + col_s + h * 64, w0);
+            tmem_ld32(t_row + col_s + h * 64 + 32, w1);
+            if (masked_tile) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                if (kv0 + h * 64 + i >= lim) w0[i] = __float_as_uint(-INFINITY);
+                if (kv0 + h * 64 + 32 + i >= lim) w1[i] = __float_as_uint(-INFINITY);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t* src = (i < 16) ? w0 : w1;
+              const int e = (i & 15) * 2;
+              const float2 tt = __ffma2_rn(make_float2(u2f(src[e]), u2f(src[e + 1])), c2, nm2);
+              const float p0 = ex2_mufu(tt.x), p1 = ex2_mufu(tt.y);
+              sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            __syncwarp();
+            tmem_st32(t_row + col_s + h * 32, pk);
+          }
+        } else {
+          // scale <= 0: two passes over TMEM, the max of s*c through min/max
+          // of the raw scores, and masked columns zeroed explicitly (with
+          // scale 0, -inf * 0 would be NaN).
+          float mraw = (c == 0.f) ? -INFINITY : INFINITY;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(t_row + L::kColO + c * 32, r);
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t w[32];
+            __syncwarp();
+            tmem_ld32(t_row + col_s + cb * 32, w);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(u2f(r[i]) * alpha);
-            tmem_st32(t_row + L::kColO + c * 32, r);
+            for (int i = 0; i < 32; ++i) {
+              const bool dead = kv0 + cb * 32 + i >= lim;
+              const float x = u2f(w[i]);
+              if (c == 0.f)
+                mraw = dead ? mraw : fmaxf(mraw, 0.f * x);
+              else
+                mraw = dead ? mraw : fminf(mraw, x);
+            }
+          }
+          const bool none = (c == 0.f) ? (mraw == -INFINITY) : (mraw == INFINITY);
+          update_max(none ? -INFINITY : (c == 0.f ? 0.f : mraw * c));
+          const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t w0[32], w1[32], pk[32];
+            __syncwarp();
+            tmem_ld32(t_row + col_s + h * 64, w0);
+            tmem_ld32(t_row + col_s + h * 64 + 32, w1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t* src = (i < 16) ? w0 : w1;
+              const int e = (i & 15) * 2, col = kv0 + h * 64 + 2 * i;
+              float p0 = ex2_mufu(fmaf(u2f(src[e]), c, neg_m));
+              float p1 = ex2_mufu(fmaf(u2f(src[e + 1]), c, neg_m));
+              if (col >= lim) p0 = 0.f;
+              if (col + 1 >= lim) p1 = 0.f;
+              sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            __syncwarp();
+            tmem_st32(t_row + col_s + h * 32, pk);
           }
         }
-        __syncwarp();
-        tmem_st32(t_row + sb * 128, *reinterpret_cast<const uint32_t(*)[32]>(&p[0]));
-        tmem_st32(t_row + sb * 128 + 32, *reinterpret_cast<const uint32_t(*)[32]>(&p[32]));
+        l_run = l_run * alpha + (sum2.x + sum2.y);
+        // O_t is stable here: S_t(j) completing implies GEMM 2 of tile j-1 has
+        // completed, and GEMM 2 of tile j waits for this thread's P.
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(t_row + col_o + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
+            tmem_st32(t_row + col_o + cc * 32, o);
+          }
+        }
         tc_fence_before();
-        mbar_arrive(bar(L::kBarPFull + sb));
-        ++g;
+        mbar_arrive(bar(L::kBarPFull + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l)
-      while (o_seen < g) {
-        if (!warp_wait(bar(L::kBarO), o_seen & 1, abort_flag)) { ok = false; break; }
-        ++o_seen;
-      }
-      if (!ok) break;
+      if (!warp_wait(bar(L::kBarOFinal + t), nu & 1, abort_flag)) { ok = false; break; }
+      ++nu;
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
       const bool row_ok = q_row < a.Sq;
@@ -388,13 +466,13 @@ __global__ void __launch_bounds__(192, 1)
           reinterpret_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.Sq + (row_ok ? q_row : 0)) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
+        uint32_t v[32];
         __syncwarp();  // reconverge after the per-row store before the warp-wide load
-        tmem_ld32(t_row + L::kColO + c * 32, r);
+        tmem_ld32(t_row + col_o + c * 32, v);
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(u2f(r[2 * i]) * inv_l, u2f(r[2 * i + 1]) * inv_l);
+          w[i] = pack_bf16x2(u2f(v[2 * i]) * inv_l, u2f(v[2 * i + 1]) * inv_l);
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -404,13 +482,13 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (row_ok) a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       tc_fence_before();
-      mbar_arrive(bar(L::kBarOFree));
+      mbar_arrive(bar(L::kBarOFree + t));
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -438,8 +516,8 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const int sms = info.sm_count;
   int grid;
   if (a.causal) {
-    // contiguous chunks of an even number of units: a long and a short q tile
-    // of the same head pair up, so chunks carry near-equal work
+    // contiguous chunks of an even number of units: a long and a short tile pair
+    // of the same head come together, so chunks carry near-equal work
     int chunk = (a.n_units + sms - 1) / sms;
     if (chunk > 1 && (chunk & 1)) ++chunk;
     a.chunk = chunk;
@@ -449,7 +527,7 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     grid = a.n_units < sms ? a.n_units : sms;
   }
   record_timing(false, stream);
-  fwd_kernel<D><<<grid, 192, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  fwd_kernel<D><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   record_timing(true, stream);
   note_launches(1);

@@ -37,6 +37,7 @@ struct FwdArgs {
   int causal;
   float scale_log2;  // scale * log2(e)
   int n_qtiles;
+  int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
   int n_units;
   int chunk;  // > 0: CTA c takes units [c*chunk, (c+1)*chunk); 0: round robin
 };
