@@ -446,14 +446,12 @@ __global__ void __launch_bounds__(320, 1)
         // queries c with iq*64 + c < kv are masked (causal)
         const int causal_lim = a.causal ? kv - iq * kQB : -1;
         float p[kQB];
+        {
+          uint32_t v[kQB];
+          tmem_ld64(t_row + L::kColS + (it & 1) * kQB, v);  // one round trip
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColS + (it & 1) * kQB + c2 * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = c2 * 32 + e;
-            const float x = ex2_mufu(u2f(v[e]) * a.scale_log2 - s_lse2[c]);
+          for (int c = 0; c < kQB; ++c) {
+            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, -s_lse2[c]));
             p[c] = (row_dead || c < causal_lim) ? 0.f : x;
           }
         }
@@ -467,10 +465,11 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive(bar(L::kBarPReady));
         if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        uint32_t dpv[kQB];
+        tmem_ld64(t_row + L::kColDP, dpv);  // one round trip
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColDP + c2 * 32, v);
+          const uint32_t* v = dpv + c2 * 32;
           uint32_t wbuf[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -515,13 +514,12 @@ __global__ void __launch_bounds__(320, 1)
         // the previous block's bulk reduce must have finished reading the staging tile
         if (r == 0) bulk_wait_read();
         group_sync(2);
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColDQ + c2 * 32, v);
+        {
+          uint32_t v[kQB];
+          tmem_ld64(t_row + L::kColDQ, v);  // one round trip
           if (r < D) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage_dq[(c2 * 32 + e) * D + r] = u2f(v[e]);
+            for (int e = 0; e < kQB; ++e) stage_dq[e * D + r] = u2f(v[e]);
           }
         }
         tc_fence_before();
