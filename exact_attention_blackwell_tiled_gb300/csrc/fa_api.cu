@@ -254,6 +254,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.Sq_pad = a.n_qtiles * kTile;
   a.n_ktiles = (Sk + kTile - 1) / kTile;
   a.n_units = B * Hkv * a.n_ktiles;
+  // longest-first snake when the streamed queries and output gradients
+  // (q, dO) fit comfortably in L2
+  a.snake = (causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
   a.causal = causal ? 1 : 0;
   a.deterministic = deterministic ? 1 : 0;
   a.scale = scale;

@@ -209,10 +209,29 @@ struct BwdUnit {
   int bhk, j, b, hk, lo, n_blk, n_it;
 };
 
+// The r-th unit this CTA processes (-1 when it has no more).  Units are either
+// head-major (u = bhk * n_ktiles + j, round robin, so CTAs running together
+// share the queries of few heads in L2) or, when those fit in L2 anyway,
+// ordered by ascending kv tile (the longest causal units first) and dealt in a
+// snake so that per-CTA work evens out.  Either order lists kv tile j-1 of a
+// head before tile j, which the deterministic dQ chain relies on.
+__device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
+  const int k = a.snake ? r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x
+                                                         : (int)blockIdx.x)
+                        : (int)blockIdx.x + r * (int)gridDim.x;
+  return k < a.n_units ? k : -1;
+}
+
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) {
   BwdUnit w;
-  w.bhk = u / a.n_ktiles;
-  w.j = u - w.bhk * a.n_ktiles;
+  if (a.snake) {
+    const int nbhk = a.B * a.Hkv;
+    w.j = u / nbhk;
+    w.bhk = u - w.j * nbhk;
+  } else {
+    w.bhk = u / a.n_ktiles;
+    w.j = u - w.bhk * a.n_ktiles;
+  }
   w.b = w.bhk / a.Hkv;
   w.hk = w.bhk - w.b * a.Hkv;
   w.lo = bwd_qblk_lo(a, w.j);
@@ -282,7 +301,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
+      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
         const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVEmpty), (unit & 1) ^ 1, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVTileBytes);
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(320, 1)
                   kIdS, kk > 0 ? 1u : 0u);
         umma_commit(bar(L::kBarDPFull));
       };
-      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
+      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
         const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -426,7 +445,7 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* ds_row = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
       const BwdUnit w = bwd_unit(a, u, group);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= a.Sk;
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(320, 1)
     float* stage_dq = reinterpret_cast<float*>(smem + L::kOffDQ);
     uint32_t it = 0, unit = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x, ++unit) {
+    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
       const BwdUnit w = bwd_unit(a, u, group);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;

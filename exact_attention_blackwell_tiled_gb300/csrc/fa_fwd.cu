@@ -69,30 +69,37 @@ struct FwdLayout {
   static constexpr uint32_t kColO = 256;
 };
 
-struct UnitRange {
-  int first, stride, end;
-};
-
-__device__ __forceinline__ UnitRange cta_units(const FwdArgs& a) {
-  UnitRange r;
-  if (a.chunk > 0) {
-    r.first = blockIdx.x * a.chunk;
-    r.stride = 1;
-    r.end = min(a.n_units, r.first + a.chunk);
+// The r-th unit this CTA processes (-1 when it has no more).  Every role of
+// the CTA walks the same sequence.
+__device__ __forceinline__ int cta_unit(const FwdArgs& a, int r) {
+  int k;
+  if (a.sched == 1) {
+    if (r >= a.chunk) return -1;
+    k = blockIdx.x * a.chunk + r;
+  } else if (a.sched == 2) {
+    // boustrophedon: each round of gridDim.x units alternates direction, so
+    // CTAs that got a longer unit in one round get a shorter one in the next
+    k = r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
   } else {
-    r.first = blockIdx.x;
-    r.stride = gridDim.x;
-    r.end = a.n_units;
+    k = blockIdx.x + r * gridDim.x;
   }
-  return r;
+  return k < a.n_units ? k : -1;
 }
 
 // Unit u -> (flat batch*head index, tile pair p: query tiles 2p and 2p+1).
-// Units are head-major so that the CTAs running at the same time share the K/V
-// of few heads in L2.  Causal pairs alternate longest / shortest inside a head
-// so contiguous chunks carry near-equal work.
+//   sched 0 / 1: head-major, so CTAs running at the same time share the K/V of
+//                few heads in L2; causal pairs alternate longest / shortest
+//                inside a head so contiguous chunks carry near-equal work.
+//   sched 2:     longest pairs of every head first (causal work grows with the
+//                pair index), used when all K/V fit in L2.
 __device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& pair) {
   const int np = a.n_pairs;
+  if (a.sched == 2) {
+    const int BH = a.B * a.Hq;
+    pair = np - 1 - u / BH;
+    bh = u - (u / BH) * BH;
+    return;
+  }
   bh = u / np;
   const int r = u - bh * np;
   pair = a.causal ? ((r & 1) ? (r >> 1) : (np - 1 - (r >> 1))) : r;
@@ -168,7 +175,6 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const UnitRange ur = cta_units(a);
   const int group = a.Hq / a.Hkv;
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(320, 1)
         ++kv_it;
         return true;
       };
-      for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
+      for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
         int bh, pair;
         unit_coords(a, u, bh, pair);
         const int b = bh / a.Hq, h = bh - b * a.Hq;
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t p_seen[2] = {0u, 0u};  // P-ready phases consumed, per tile
       uint32_t units_t[2] = {0u, 0u};  // units with work, per tile (O-free phases)
       bool ok = true;
-      for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
+      for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
         int bh, pair;
         unit_coords(a, u, bh, pair);
         const int n[2] = {tile_kv_count(a, 2 * pair), tile_kv_count(a, 2 * pair + 1)};
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t col_s = t * kTile, col_o = L::kColO + t * D;
     uint32_t g = 0, nu = 0;  // S-full phases and units consumed by this group
     bool ok = true;
-    for (int u = ur.first; ok && u < ur.end; u += ur.stride) {
+    for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
       int bh, pair;
       unit_coords(a, u, bh, pair);
       const int qt = 2 * pair + t;
@@ -515,14 +521,22 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   a.status = status;
   const int sms = info.sm_count;
   int grid;
-  if (a.causal) {
+  const double kv_bytes = 2.0 * a.B * a.Hkv * (double)a.Sk * D * 2;
+  if (a.causal && kv_bytes <= 64.0 * (1 << 20)) {
+    // all K/V fit comfortably in L2: longest-first snake over every head
+    a.sched = 2;
+    a.chunk = 0;
+    grid = a.n_units < sms ? a.n_units : sms;
+  } else if (a.causal) {
     // contiguous chunks of an even number of units: a long and a short tile pair
     // of the same head come together, so chunks carry near-equal work
     int chunk = (a.n_units + sms - 1) / sms;
     if (chunk > 1 && (chunk & 1)) ++chunk;
+    a.sched = 1;
     a.chunk = chunk;
     grid = (a.n_units + chunk - 1) / chunk;
   } else {
+    a.sched = 0;
     a.chunk = 0;
     grid = a.n_units < sms ? a.n_units : sms;
   }

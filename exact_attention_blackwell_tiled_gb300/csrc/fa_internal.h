@@ -39,7 +39,9 @@ struct FwdArgs {
   int n_qtiles;
   int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
   int n_units;
-  int chunk;  // > 0: CTA c takes units [c*chunk, (c+1)*chunk); 0: round robin
+  int sched;  // 0: round robin over head-major units; 1: contiguous chunks of
+              // `chunk` units; 2: longest-first snake over all heads
+  int chunk;
 };
 
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -69,6 +71,7 @@ struct BwdArgs {
   int n_qblk;    // 64-row query blocks of Sq (the backward's q step)
   int n_ktiles;  // 128-row kv tiles of Sk
   int n_units;
+  int snake;     // 1: units dealt longest-first (ascending kv tile) in a snake
 };
 
 struct BwdLayout {
