@@ -19,12 +19,15 @@
 //                        dS^T = P^T * (dP^T - Delta_i)     -> bf16 in TMEM and smem
 //                        dV_j += P^T dO_i,  dK_j += dS^T Q_i  (TMEM accumulators)
 //                        dQ_i^T = K_j^T dS_i^T             (TMEM, rows = head dim)
-//                      dQ_i^T is staged in shared memory as [query][dim] fp32
-//                      and added to the accumulator with ONE bulk TMA
-//                      reduce-add per block (no per-element atomics); in the
-//                      deterministic mode those reductions run in kv-tile order
-//                      behind a per-(b, h, block) semaphore.  At the end of the
-//                      unit dK_j * scale and dV_j are written as bf16.
+//                      dQ_i^T goes from TMEM straight into the fp32
+//                      accumulator with reduction adds: thread d adds column d
+//                      of the 64 query rows, so every warp instruction covers
+//                      one 128-byte line (no shared-memory staging, which would
+//                      compete with the MMA operand reads for shared-memory
+//                      bandwidth).  In the deterministic mode each warp adds in
+//                      kv-tile order behind a per-(b, h, block) semaphore.  At
+//                      the end of the unit dK_j * scale and dV_j are written as
+//                      bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
 //
 // bwd_main warp roles (320 threads):
@@ -33,11 +36,12 @@
 //   warp 8     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
 //              block into a 3-stage ring;
 //   warp 9     TMEM owner and single-thread tcgen05.mma issuer.
-// TMEM columns: S^T/P^T double buffer [0,64) [64,128), dP^T/dS^T [128,192),
-// dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
-// MMA issue order per block i: S^T(i+1), dV(i), dK(i), dQ^T(i), dP^T(i+1), so
-// the tensor core works on the next block while the softmax warps finish this
-// one.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
+// TMEM columns: S^T double buffer [0,64) [64,128) (P^T and then dS^T, bf16,
+// replace it in place: P^T in its first 32 columns, dS^T in the last 32),
+// dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
+// MMA issue order per block i: S^T(i+1), dV(i), dP^T(i+1), dK(i), dQ^T(i): the
+// tensor core works on the next block while the softmax warps finish this one,
+// and the next dP^T is ready as soon as the softmax warps want it.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
 // block twice; lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
@@ -101,11 +105,11 @@ struct BwdSmem {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVTileBytes;
   static constexpr int kOffStage = kOffV + kKVTileBytes;
-  static constexpr int kOffDS = kOffStage + kStages * kStageBytes;  // dS^T [key][64 queries]
+  // dS^T [key][64 queries], two buffers by block parity: block i+1's dS^T is
+  // written while the dQ^T MMA of block i may still be reading block i's
+  static constexpr int kOffDS = kOffStage + kStages * kStageBytes;
   static constexpr int kDSBytes = kTile * kQB * 2;
-  static constexpr int kOffDQ = kOffDS + kDSBytes;  // dQ staging [64 queries][D] fp32
-  static constexpr int kDQBytes = kQB * D * 4;
-  static constexpr int kOffBar = kOffDQ + kDQBytes;
+  static constexpr int kOffBar = kOffDS + 2 * kDSBytes;
   static constexpr int kBarKVFull = 0, kBarKVEmpty = 1;
   static constexpr int kBarQFull = 2;                // kStages
   static constexpr int kBarQEmpty = 2 + kStages;     // kStages
@@ -119,7 +123,7 @@ struct BwdSmem {
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarDrain = kBarDKVEmpty + 1;
   static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, sem flag
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -177,21 +181,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-
-__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   dst),
-               "r"(src), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
@@ -252,7 +241,6 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
-  volatile int* sem_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8 * i; };
@@ -277,7 +265,6 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(L::kBarDKVEmpty), 128);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
-    *sem_flag = 1;
     fence_mbarrier_init();
   }
   if (warp == 9) {
@@ -349,31 +336,36 @@ __global__ void __launch_bounds__(320, 1)
       // K^T as the MN-major A operand of dQ^T: the second 64-row head-dim block
       // is the second column block of K (D = 128) or, at D = 64, the first again.
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
-      const uint32_t k_base = sbase + L::kOffK, v_base = sbase + L::kOffV;
-      const uint32_t ds_base = sbase + L::kOffDS;
+      constexpr uint32_t kHi = sdesc_hi(1024);
+      // Descriptor low words: buffers fixed for the kernel are computed once,
+      // per-block buffers once per block; each K step adds a constant.
+      const uint32_t k_lo = sdesc_lo(sbase + L::kOffK, 16), v_lo = sdesc_lo(sbase + L::kOffV, 16);
+      const uint32_t kt_lo = sdesc_lo(sbase + L::kOffK, kLboKT);
+      const uint32_t ds_lo = sdesc_lo(sbase + L::kOffDS, 1024);
       uint32_t it = 0, unit = 0;
       bool ok = true;
       auto wait_q = [&](uint32_t i) -> bool {
         return mbar_wait(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag);
       };
-      auto issue_s = [&](uint32_t i) {  // S^T(i) = K Q_i^T into buffer i % 2
-        const uint32_t q_base = sbase + stage_off(i);
+      // S^T(i) = K Q_i^T (or dP^T(i) = V dO_i^T): both operands K-major
+      auto issue_kmajor = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kColS + (i & 1) * kQB,
-                  sdesc_sw128(k_base + (kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(q_base + (kk >> 2) * L::kQBlockBytes + (kk & 3) * 32, 16, 1024),
-                  kIdS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32) >> 4;
+          const uint32_t kb = ((kk >> 2) * L::kQBlockBytes + (kk & 3) * 32) >> 4;
+          if (kk == 0)
+            umma_ss_w<0>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
+          else
+            umma_ss_w<1>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
+        }
+      };
+      auto issue_s = [&](uint32_t i) {
+        issue_kmajor(tmem + L::kColS + (i & 1) * kQB, k_lo, sdesc_lo(sbase + stage_off(i), 16));
         umma_commit(bar(L::kBarSFull + (i & 1)));
       };
-      auto issue_dp = [&](uint32_t i) {  // dP^T(i) = V dO_i^T
-        const uint32_t do_base = sbase + stage_off(i) + L::kQTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kColDP,
-                  sdesc_sw128(v_base + (kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(do_base + (kk >> 2) * L::kQBlockBytes + (kk & 3) * 32, 16, 1024),
-                  kIdS, kk > 0 ? 1u : 0u);
+      auto issue_dp = [&](uint32_t i) {
+        issue_kmajor(tmem + L::kColDP, v_lo,
+                     sdesc_lo(sbase + stage_off(i) + L::kQTileBytes, 16));
         umma_commit(bar(L::kBarDPFull));
       };
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
@@ -395,7 +387,10 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int t = 0; t < w.n_it; ++t, ++it) {
           const uint32_t q_base = sbase + stage_off(it);
-          const uint32_t do_base = q_base + L::kQTileBytes;
+          // Q and dO of this block as MN-major B operands (K = queries)
+          const uint32_t q_mn_lo = sdesc_lo(q_base, L::kQBlockBytes);
+          const uint32_t do_mn_lo = sdesc_lo(q_base + L::kQTileBytes, L::kQBlockBytes);
+          const uint32_t s_col = L::kColS + (it & 1) * kQB;
           if (t + 1 < w.n_it) {
             if (!wait_q(it + 1)) { ok = false; break; }
             tc_fence_after();
@@ -406,16 +401,17 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kQB / 16; ++kk)  // dV += P^T dO  (K = queries)
-            umma_ts(tmem + L::kColDV, tmem + L::kColS + (it & 1) * kQB + kk * 8,
-                    sdesc_sw128(do_base + kk * 16 * 128, L::kQBlockBytes, 1024), kIdAcc,
-                    (t > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_w(tmem + L::kColDV, tmem + s_col + kk * 8, do_mn_lo + ((kk * 16 * 128) >> 4),
+                      kHi, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
           if (!mbar_wait(bar(L::kBarDSReady), it & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
+          // the softmax warps have read dP^T(it): compute the next block's dP^T
+          // first, so they can start on it while dK / dQ^T run
+          if (t + 1 < w.n_it) issue_dp(it + 1);
 #pragma unroll
           for (int kk = 0; kk < kQB / 16; ++kk)  // dK += dS^T Q
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8,
-                    sdesc_sw128(q_base + kk * 16 * 128, L::kQBlockBytes, 1024), kIdAcc,
-                    (t > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_w(tmem + L::kColDK, tmem + s_col + 32 + kk * 8,
+                      q_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(L::kBarQEmpty + it % L::kStages));
           // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
           // previous block has emptied the dQ^T columns
@@ -424,12 +420,18 @@ __global__ void __launch_bounds__(320, 1)
             break;
           }
           tc_fence_after();
+          {
+            const uint32_t dsb_lo = ds_lo + (((it & 1) * L::kDSBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ss(tmem + L::kColDQ, sdesc_sw128(k_base + kk * 16 * 128, kLboKT, 1024),
-                    sdesc_sw128(ds_base + kk * 16 * 128, 1024, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t ko = (kk * 16 * 128) >> 4;
+              if (kk == 0)
+                umma_ss_w<0>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
+              else
+                umma_ss_w<1>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
+            }
+          }
           umma_commit(bar(L::kBarDQFull));
-          if (t + 1 < w.n_it) issue_dp(it + 1);
         }
         if (!ok) break;
         umma_commit(bar(L::kBarKVEmpty));
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ P^T / dS^T
     const int r = threadIdx.x;  // key row of the kv tile == TMEM lane
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-    uint8_t* ds_row = smem + L::kOffDS + r * 128;
+    uint8_t* ds_rows = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
@@ -462,6 +464,7 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
+        uint8_t* ds_row = ds_rows + (it & 1) * L::kDSBytes;
         // queries c with iq*64 + c < kv are masked (causal)
         const int causal_lim = a.causal ? kv - iq * kQB : -1;
         float p[kQB];
@@ -497,8 +500,10 @@ __global__ void __launch_bounds__(320, 1)
             const float d1 = p[c + 1] * (u2f(v[2 * e + 1]) - s_delta[c + 1]);
             wbuf[e] = pack_bf16x2(d0, d1);
           }
-          // packed over the dP^T columns this thread has already read
-          tmem_st16(t_row + L::kColDP + c2 * 16, wbuf);
+          // packed into the S^T buffer of this block, next to P^T (its S^T
+          // columns were consumed by P), so the dP^T columns are free for the
+          // next block as soon as they have been read
+          tmem_st16(t_row + L::kColS + (it & 1) * kQB + 32 + c2 * 16, wbuf);
           // shared memory, 128-byte swizzle: [key row][64 queries]
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -518,7 +523,6 @@ __global__ void __launch_bounds__(320, 1)
     const int r = threadIdx.x - 128;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
     const int wq = warp - 4;
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
-    float* stage_dq = reinterpret_cast<float*>(smem + L::kOffDQ);
     uint32_t it = 0, unit = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
@@ -530,48 +534,47 @@ __global__ void __launch_bounds__(320, 1)
         ok = group_all(warp_wait_b(bar(L::kBarDQFull), it & 1, abort_flag), 2);
         if (!ok) break;
         tc_fence_after();
-        // the previous block's bulk reduce must have finished reading the staging tile
-        if (r == 0) bulk_wait_read();
-        group_sync(2);
-        {
-          uint32_t v[kQB];
-          tmem_ld64(t_row + L::kColDQ, v);  // one round trip
-          if (r < D) {
-#pragma unroll
-            for (int e = 0; e < kQB; ++e) stage_dq[e * D + r] = u2f(v[e]);
-          }
-        }
+        // Row r of dQ^T (head-dim index r, 64 queries) goes straight from TMEM
+        // to the fp32 accumulator: for each query the 32 lanes of a warp add
+        // 32 consecutive floats, one 128-byte line per instruction.
+        uint32_t v[kQB];
+        tmem_ld64(t_row + L::kColDQ, v);  // one round trip
         tc_fence_before();
         mbar_arrive(bar(L::kBarDQEmpty));
-        fence_proxy_async_smem();
-        group_sync(2);
-        if (r == 0) {
-          float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D;
-          int good = 1;
-          if (a.deterministic) {
-            // kv tiles add their part of block iq in ascending order j
-            int* sem = a.sem + (size_t)bh * a.n_qblk + iq;
+        float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
+        constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
+        int good = 1;
+        if (a.deterministic && wq < kAddWarps) {
+          // kv tiles add into block iq in ascending order: the semaphore counts
+          // finished adding warps, so tile j starts once it reaches j * kAddWarps
+          int* sem = a.sem + (size_t)bh * a.n_qblk + iq;
+          if (lane == 0) {
             const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(sem) != w.j) {
+            while (ld_acquire(sem) < w.j * kAddWarps) {
               if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
                 *abort_flag = 1;
                 good = 0;
                 break;
               }
             }
-            if (good) {
-              bulk_reduce_add_f32(dst, smem_u32(stage_dq), kQB * D * 4);
-              bulk_wait_all();
-              __threadfence();
-              atomicAdd(sem, 1);
-            }
-          } else {
-            bulk_reduce_add_f32(dst, smem_u32(stage_dq), kQB * D * 4);
           }
-          *sem_flag = good;
+          good = __shfl_sync(0xffffffffu, good, 0);
+          __syncwarp();
         }
-        group_sync(2);
-        if (!*sem_flag) { ok = false; break; }
+        if (good && r < D) {
+#pragma unroll
+          for (int e = 0; e < kQB; ++e)
+            asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
+                         "f"(u2f(v[e]))
+                         : "memory");
+        }
+        if (a.deterministic && wq < kAddWarps && good) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(a.sem + (size_t)bh * a.n_qblk + iq, 1);
+        }
+        ok = group_all(good != 0, 2);
+        if (!ok) break;
       }
       if (!ok) break;
       // ---- dK, dV epilogue for key row kv
@@ -613,8 +616,6 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarDKVEmpty));
     }
-    // outstanding bulk reductions must finish before the kernel ends
-    if (r == 0) bulk_wait_all();
   }
 
   tc_fence_before();
