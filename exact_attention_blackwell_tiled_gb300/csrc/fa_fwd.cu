@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTile, D, false, true);
+      constexpr uint32_t kHi = sdesc_hi(1024);  // SBO 1024 B, version 1, 128B swizzle
       uint32_t kv_it = 0, q_it = 0;
       uint32_t p_seen[2] = {0u, 0u};  // P-ready phases consumed, per tile
       uint32_t units_t[2] = {0u, 0u};  // units with work, per tile (O-free phases)
@@ -280,21 +281,25 @@ __global__ void __launch_bounds__(320, 1)
                 break;
               }
               tc_fence_after();
+              const uint32_t v_lo = sdesc_lo(v_base, L::kBlockBytes);
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
-                umma_ts(tmem + L::kColO + t * D, tmem + t * kTile + kk * 8,
-                        sdesc_sw128(v_base + kk * 16 * 128, L::kBlockBytes, 1024), kIdescO,
-                        (j > 1 || kk > 0) ? 1u : 0u);
+                umma_ts_w(tmem + L::kColO + t * D, tmem + t * kTile + kk * 8,
+                          v_lo + ((kk * 16 * 128) >> 4), kHi, kIdescO,
+                          (j > 1 || kk > 0) ? 1u : 0u);
               if (j == n[t]) umma_commit(bar(L::kBarOFinal + t));
             }
             if (j < n[t]) {
               // GEMM 1: S_t = Q_t K_j^T
-              const uint32_t qb = q_base + t * L::kTileBytes;
+              const uint32_t q_lo = sdesc_lo(q_base + t * L::kTileBytes, 16);
+              const uint32_t k_lo = sdesc_lo(k_base, 16);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * L::kBlockBytes + (kk & 3) * 32;
-                umma_ss(tmem + t * kTile, sdesc_sw128(qb + off, 16, 1024),
-                        sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                const uint32_t off = ((kk >> 2) * L::kBlockBytes + (kk & 3) * 32) >> 4;
+                if (kk == 0)
+                  umma_ss_w<0>(tmem + t * kTile, q_lo + off, kHi, k_lo + off, kHi, kIdescS);
+                else
+                  umma_ss_w<1>(tmem + t * kTile, q_lo + off, kHi, k_lo + off, kHi, kIdescS);
               }
               umma_commit(bar(L::kBarSFull + t));
             }
