@@ -30,18 +30,32 @@
 //                      bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
 //
-// bwd_main warp roles (320 threads):
-//   warps 0-3  P^T / dS^T, one key row per thread (TMEM lane);
-//   warps 4-7  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
-//   warp 8     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
-//              block into a 3-stage ring;
-//   warp 9     TMEM owner and single-thread tcgen05.mma issuer.
-// TMEM columns: S^T double buffer [0,64) [64,128) (P^T and then dS^T, bf16,
-// replace it in place: P^T in its first 32 columns, dS^T in the last 32),
+// bwd_main warp roles (480 threads):
+//   warps 0-7   P^T / dS^T: warp w serves key rows 32*(w%4).. (its TMEM lanes)
+//               and query columns 32*(w/4).. of the block, so each SM
+//               sub-partition runs two of them and one's latencies hide
+//               behind the other's work;
+//   warps 8-11  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
+//   warp 12     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
+//               block into a 3-stage ring;
+//   warp 13     TMEM owner; one thread issues S^T and dP^T;
+//   warp 14     one thread issues dV, dK and dQ^T.
+// TMEM columns: S^T double buffer [0,64) [64,128); P^T and dS^T (bf16 pairs)
+// replace it in place: query columns 32h..32h+31 of S^T are read by the warps
+// of half h, which then write their 16 columns of P^T and 16 of dS^T over
+// them (P^T at 32h, dS^T at 32h+16), so the two halves never touch each
+// other's columns;
 // dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
-// MMA issue order per block i: S^T(i+1), dV(i), dP^T(i+1), dK(i), dQ^T(i): the
-// tensor core works on the next block while the softmax warps finish this one,
-// and the next dP^T is ready as soon as the softmax warps want it.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
+// Two issuing threads: a thread that has MMAs queued and then waits on a
+// barrier only continues once the tensor core has taken those MMAs, so a lone
+// issuer lets the tensor core run dry at every wait.  The score side (S^T as
+// soon as Q_i has landed and its S^T buffer is free, dP^T as soon as the
+// softmax warps have read the previous one) and the gradient side (dV, dK, dQ^T
+// as the softmax warps publish P^T and dS^T) wait on different events, and
+// each one's waits are covered by the MMAs the other has queued.  Buffers that
+// one side fills and the other reads are handed back through their own
+// barriers: an S^T buffer is free once dK of the block that used it is done,
+// a shared dS^T buffer once its dQ^T is done.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
 // block twice; lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
@@ -51,6 +65,15 @@
 namespace fa {
 
 constexpr int kQB = 64;  // query rows per backward block
+
+// bwd_main warp roles
+constexpr int kBwdSmxWarps = 8;     // warps 0-7: P^T / dS^T
+constexpr int kBwdDrainWarp0 = 8;   // warps 8-11: dQ drain, dK/dV epilogue
+constexpr int kBwdTmaWarp = 12;
+constexpr int kBwdScoreWarp = 13;   // TMEM owner, S^T / dP^T issuer
+constexpr int kBwdGradWarp = 14;    // dV / dK / dQ^T issuer
+constexpr int kBwdThreads = 32 * (kBwdGradWarp + 1);
+constexpr int kBwdSmxThreads = 32 * kBwdSmxWarps;
 
 // ------------------------------------------------------------------ preprocess
 
@@ -114,15 +137,19 @@ struct BwdSmem {
   static constexpr int kBarQFull = 2;                // kStages
   static constexpr int kBarQEmpty = 2 + kStages;     // kStages
   static constexpr int kBarSFull = 2 + 2 * kStages;  // 2
-  static constexpr int kBarPReady = kBarSFull + 2;
-  static constexpr int kBarDPFull = kBarPReady + 1;
-  static constexpr int kBarDSReady = kBarDPFull + 1;
-  static constexpr int kBarDQFull = kBarDSReady + 1;
+  // P^T / dS^T published, one barrier per block parity: a waiter may lag the
+  // softmax warps by a block, never by two blocks of the same parity
+  static constexpr int kBarPReady = kBarSFull + 2;   // 2
+  static constexpr int kBarDPFull = kBarPReady + 2;
+  static constexpr int kBarDSReady = kBarDPFull + 1;  // 2
+  static constexpr int kBarDQFull = kBarDSReady + 2;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQEmpty + 1;
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
-  static constexpr int kBarDrain = kBarDKVEmpty + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
+  static constexpr int kBarDSFree = kBarSFree + 2;     // 2: shared dS^T buffer read by dQ^T
+  static constexpr int kBarDrain = kBarDSFree + 2;     // 2: one per issuer
+  static constexpr int kNumBars = kBarDrain + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
@@ -230,7 +257,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
@@ -250,28 +277,34 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarKVFull), 1);
-    mbar_init(bar(L::kBarKVEmpty), 1);
+    mbar_init(bar(L::kBarKVEmpty), 2);  // both issuers commit
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
       mbar_init(bar(L::kBarQEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
-    mbar_init(bar(L::kBarPReady), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kBarPReady + s), kBwdSmxThreads);
+      mbar_init(bar(L::kBarDSReady + s), kBwdSmxThreads);
+    }
     mbar_init(bar(L::kBarDPFull), 1);
-    mbar_init(bar(L::kBarDSReady), 128);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKVFull), 1);
     mbar_init(bar(L::kBarDKVEmpty), 128);
-    mbar_init(bar(L::kBarDrain), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kBarSFree + s), 1);
+      mbar_init(bar(L::kBarDSFree + s), 1);
+      mbar_init(bar(L::kBarDrain + s), 1);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 9) {
+  if (warp == kBwdScoreWarp) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kBwdTmaWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -283,7 +316,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
 
-  if (warp == 8) {
+  if (warp == kBwdTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0, unit = 0;
@@ -327,8 +360,8 @@ __global__ void __launch_bounds__(320, 1)
       for (uint32_t n = (it > (uint32_t)L::kStages ? it - L::kStages : 0); n < it; ++n)
         drain_wait_b(bar(L::kBarQFull + n % L::kStages), (n / L::kStages) & 1);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= kBwdScoreWarp) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kQB, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, false, true);   // dV, dK
@@ -337,90 +370,105 @@ __global__ void __launch_bounds__(320, 1)
       // is the second column block of K (D = 128) or, at D = 64, the first again.
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
       constexpr uint32_t kHi = sdesc_hi(1024);
-      // Descriptor low words: buffers fixed for the kernel are computed once,
-      // per-block buffers once per block; each K step adds a constant.
-      const uint32_t k_lo = sdesc_lo(sbase + L::kOffK, 16), v_lo = sdesc_lo(sbase + L::kOffV, 16);
-      const uint32_t kt_lo = sdesc_lo(sbase + L::kOffK, kLboKT);
-      const uint32_t ds_lo = sdesc_lo(sbase + L::kOffDS, 1024);
+      const bool score_side = (warp == kBwdScoreWarp);
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      auto wait_q = [&](uint32_t i) -> bool {
-        return mbar_wait(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag);
-      };
-      // S^T(i) = K Q_i^T (or dP^T(i) = V dO_i^T): both operands K-major
-      auto issue_kmajor = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = ((kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32) >> 4;
-          const uint32_t kb = ((kk >> 2) * L::kQBlockBytes + (kk & 3) * 32) >> 4;
-          if (kk == 0)
-            umma_ss_w<0>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
-          else
-            umma_ss_w<1>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
-        }
-      };
-      auto issue_s = [&](uint32_t i) {
-        issue_kmajor(tmem + L::kColS + (i & 1) * kQB, k_lo, sdesc_lo(sbase + stage_off(i), 16));
-        umma_commit(bar(L::kBarSFull + (i & 1)));
-      };
-      auto issue_dp = [&](uint32_t i) {
-        issue_kmajor(tmem + L::kColDP, v_lo,
-                     sdesc_lo(sbase + stage_off(i) + L::kQTileBytes, 16));
-        umma_commit(bar(L::kBarDPFull));
-      };
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
         const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // dV / dK accumulators are free once the previous unit's epilogue has read
-        // them; waited right before this unit's first dV MMA
-        auto wait_dkv_free = [&]() -> bool {
-          return unit == 0 || mbar_wait(bar(L::kBarDKVEmpty), (unit - 1) & 1, abort_flag);
-        };
-        if (w.n_it == 0) {
-          if (!wait_dkv_free()) { ok = false; break; }
-        } else {
-          if (!wait_q(it)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(it);
-          issue_dp(it);
-        }
-        for (int t = 0; t < w.n_it; ++t, ++it) {
-          const uint32_t q_base = sbase + stage_off(it);
-          // Q and dO of this block as MN-major B operands (K = queries)
-          const uint32_t q_mn_lo = sdesc_lo(q_base, L::kQBlockBytes);
-          const uint32_t do_mn_lo = sdesc_lo(q_base + L::kQTileBytes, L::kQBlockBytes);
-          const uint32_t s_col = L::kColS + (it & 1) * kQB;
-          if (t + 1 < w.n_it) {
-            if (!wait_q(it + 1)) { ok = false; break; }
+        if (score_side) {
+          // ---- S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, both operands K-major
+          const uint32_t k_lo = sdesc_lo(sbase + L::kOffK, 16);
+          const uint32_t v_lo = sdesc_lo(sbase + L::kOffV, 16);
+          auto issue_kmajor = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ka = ((kk >> 2) * L::kKVBlockBytes + (kk & 3) * 32) >> 4;
+              const uint32_t kb = ((kk >> 2) * L::kQBlockBytes + (kk & 3) * 32) >> 4;
+              if (kk == 0)
+                umma_ss_w<0>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
+              else
+                umma_ss_w<1>(d_tmem, a_lo + ka, kHi, b_lo + kb, kHi, kIdS);
+            }
+          };
+          for (int t = 0; t < w.n_it; ++t, ++it) {
+            const uint32_t q_base = sbase + stage_off(it);
+            if (!mbar_wait(bar(L::kBarQFull + it % L::kStages), (it / L::kStages) & 1,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
+            // the S^T buffer of block it-2 is free once its dV and dK are done
+            if (it >= 2 && !mbar_wait(bar(L::kBarSFree + (it & 1)), ((it >> 1) - 1) & 1,
+                                      abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            issue_s(it + 1);
+            issue_kmajor(tmem + L::kColS + (it & 1) * kQB, k_lo, sdesc_lo(q_base, 16));
+            umma_commit(bar(L::kBarSFull + (it & 1)));
+            // the dP^T columns are free once the softmax warps have read dP^T(it-1)
+            if (it >= 1 && !mbar_wait(bar(L::kBarDSReady + ((it - 1) & 1)), ((it - 1) >> 1) & 1,
+                                      abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_kmajor(tmem + L::kColDP, v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
+            umma_commit(bar(L::kBarDPFull));
           }
-          if (!mbar_wait(bar(L::kBarPReady), it & 1, abort_flag)) { ok = false; break; }
-          if (t == 0 && !wait_dkv_free()) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kQB / 16; ++kk)  // dV += P^T dO  (K = queries)
-            umma_ts_w(tmem + L::kColDV, tmem + s_col + kk * 8, do_mn_lo + ((kk * 16 * 128) >> 4),
-                      kHi, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
-          if (!mbar_wait(bar(L::kBarDSReady), it & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          // the softmax warps have read dP^T(it): compute the next block's dP^T
-          // first, so they can start on it while dK / dQ^T run
-          if (t + 1 < w.n_it) issue_dp(it + 1);
-#pragma unroll
-          for (int kk = 0; kk < kQB / 16; ++kk)  // dK += dS^T Q
-            umma_ts_w(tmem + L::kColDK, tmem + s_col + 32 + kk * 8,
-                      q_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc, (t > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(L::kBarQEmpty + it % L::kStages));
-          // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
-          // previous block has emptied the dQ^T columns
-          if (it > 0 && !mbar_wait(bar(L::kBarDQEmpty), (it - 1) & 1, abort_flag)) {
+          // K and V may be replaced once both sides are done with them
+          if (ok) umma_commit(bar(L::kBarKVEmpty));
+        } else {
+          // ---- dV += P^T dO, dK += dS^T Q (A from TMEM), dQ^T = K^T dS^T
+          const uint32_t kt_lo = sdesc_lo(sbase + L::kOffK, kLboKT);
+          const uint32_t ds_lo = sdesc_lo(sbase + L::kOffDS, 1024);
+          // dV / dK accumulators are free once the previous unit's epilogue
+          // has read them
+          if (unit > 0 && !mbar_wait(bar(L::kBarDKVEmpty), (unit - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          {
+          for (int t = 0; t < w.n_it; ++t, ++it) {
+            const uint32_t q_base = sbase + stage_off(it);
+            // Q and dO of this block as MN-major B operands (K = queries)
+            const uint32_t q_mn_lo = sdesc_lo(q_base, L::kQBlockBytes);
+            const uint32_t do_mn_lo = sdesc_lo(q_base + L::kQTileBytes, L::kQBlockBytes);
+            const uint32_t s_col = L::kColS + (it & 1) * kQB;
+            if (!mbar_wait(bar(L::kBarPReady + (it & 1)), (it >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // query columns 16kk..16kk+15 of P^T / dS^T: half kk/2 of the block
+#pragma unroll
+            for (int kk = 0; kk < kQB / 16; ++kk)  // dV += P^T dO  (K = queries)
+              umma_ts_w(tmem + L::kColDV, tmem + s_col + (kk >> 1) * 32 + (kk & 1) * 8,
+                        do_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+            if (!mbar_wait(bar(L::kBarDSReady + (it & 1)), (it >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kQB / 16; ++kk)  // dK += dS^T Q
+              umma_ts_w(tmem + L::kColDK, tmem + s_col + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                        q_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+            // S^T, dP^T (done before the softmax warps published P^T / dS^T),
+            // dV and dK of this block are complete: the stage and the S^T buffer
+            // can be reused
+            umma_commit(bar(L::kBarQEmpty + it % L::kStages));
+            umma_commit(bar(L::kBarSFree + (it & 1)));
+            // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
+            // previous block has emptied the dQ^T columns
+            if (it > 0 && !mbar_wait(bar(L::kBarDQEmpty), (it - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             const uint32_t dsb_lo = ds_lo + (((it & 1) * L::kDSBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -430,20 +478,25 @@ __global__ void __launch_bounds__(320, 1)
               else
                 umma_ss_w<1>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
             }
+            umma_commit(bar(L::kBarDQFull));
+            umma_commit(bar(L::kBarDSFree + (it & 1)));
           }
-          umma_commit(bar(L::kBarDQFull));
+          if (ok) {
+            umma_commit(bar(L::kBarKVEmpty));
+            umma_commit(bar(L::kBarDKVFull));
+          }
         }
-        if (!ok) break;
-        umma_commit(bar(L::kBarKVEmpty));
-        umma_commit(bar(L::kBarDKVFull));
       }
-      umma_commit(bar(L::kBarDrain));
-      drain_wait_b(bar(L::kBarDrain), 0);
+      umma_commit(bar(L::kBarDrain + (score_side ? 0 : 1)));
+      drain_wait_b(bar(L::kBarDrain + (score_side ? 0 : 1)), 0);
     }
-  } else if (warp < 4) {
+  } else if (warp < kBwdSmxWarps) {
     // ------------------------------------------------------------ P^T / dS^T
-    const int r = threadIdx.x;  // key row of the kv tile == TMEM lane
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter.. = key rows
+    const int half = warp >> 2;    // query columns 32*half..
+    const int r = quarter * 32 + lane;
+    const int c0 = half * 32;
+    const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* ds_rows = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
     bool ok = true;
@@ -454,74 +507,95 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
-        const float* s_lse2 =
-            reinterpret_cast<const float*>(smem + stage_off(it) + 2 * L::kQTileBytes);
-        const float* s_delta = s_lse2 + kQB;
+        const float4* s_lse2 = reinterpret_cast<const float4*>(
+            smem + stage_off(it) + 2 * L::kQTileBytes + c0 * 4);
+        const float4* s_delta = s_lse2 + kQB / 4;
         if (!warp_wait_b(bar(L::kBarQFull + it % L::kStages), (it / L::kStages) & 1,
-                         abort_flag) ||
-            !warp_wait_b(bar(L::kBarSFull + (it & 1)), (it >> 1) & 1, abort_flag)) {
+                         abort_flag)) {
+          ok = false;
+          break;
+        }
+        // this warp's 32 LSE2 values, loaded while S^T is still being computed
+        float lse[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = s_lse2[q];
+          lse[4 * q] = x.x, lse[4 * q + 1] = x.y, lse[4 * q + 2] = x.z, lse[4 * q + 3] = x.w;
+        }
+        if (!warp_wait_b(bar(L::kBarSFull + (it & 1)), (it >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t* ds_row = ds_rows + (it & 1) * L::kDSBytes;
+        const uint32_t s_col = L::kColS + (it & 1) * kQB + c0;  // this warp's S^T columns
         // queries c with iq*64 + c < kv are masked (causal)
-        const int causal_lim = a.causal ? kv - iq * kQB : -1;
-        float p[kQB];
+        const int causal_lim = a.causal ? kv - iq * kQB - c0 : -1;
+        float p[32];
         {
-          uint32_t v[kQB];
-          tmem_ld64(t_row + L::kColS + (it & 1) * kQB, v);  // one round trip
+          uint32_t v[32];
+          tmem_ld32(t_row + s_col, v);
 #pragma unroll
-          for (int c = 0; c < kQB; ++c) {
-            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, -s_lse2[c]));
+          for (int c = 0; c < 32; ++c) {
+            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, -lse[c]));
             p[c] = (row_dead || c < causal_lim) ? 0.f : x;
           }
         }
         {
-          uint32_t wbuf[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) wbuf[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-          tmem_st32(t_row + L::kColS + (it & 1) * kQB, wbuf);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarPReady));
-        if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t dpv[kQB];
-        tmem_ld64(t_row + L::kColDP, dpv);  // one round trip
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const uint32_t* v = dpv + c2 * 32;
           uint32_t wbuf[16];
 #pragma unroll
+          for (int e = 0; e < 16; ++e) wbuf[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+          tmem_st16(t_row + s_col, wbuf);  // P^T over the first 16 of these columns
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPReady + (it & 1)));
+        float dl[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = s_delta[q];
+          dl[4 * q] = x.x, dl[4 * q + 1] = x.y, dl[4 * q + 2] = x.z, dl[4 * q + 3] = x.w;
+        }
+        if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
+        // the shared dS^T buffer of this block was last read by dQ^T(it-2)
+        if (it >= 2 &&
+            !warp_wait_b(bar(L::kBarDSFree + (it & 1)), ((it >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t wbuf[16];
+        {
+          uint32_t v[32];
+          tmem_ld32(t_row + L::kColDP + c0, v);
+#pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int c = c2 * 32 + 2 * e;
-            const float d0 = p[c] * (u2f(v[2 * e]) - s_delta[c]);
-            const float d1 = p[c + 1] * (u2f(v[2 * e + 1]) - s_delta[c + 1]);
+            const float d0 = p[2 * e] * (u2f(v[2 * e]) - dl[2 * e]);
+            const float d1 = p[2 * e + 1] * (u2f(v[2 * e + 1]) - dl[2 * e + 1]);
             wbuf[e] = pack_bf16x2(d0, d1);
           }
-          // packed into the S^T buffer of this block, next to P^T (its S^T
-          // columns were consumed by P), so the dP^T columns are free for the
-          // next block as soon as they have been read
-          tmem_st16(t_row + L::kColS + (it & 1) * kQB + 32 + c2 * 16, wbuf);
-          // shared memory, 128-byte swizzle: [key row][64 queries]
+        }
+        // dS^T over the last 16 of this warp's S^T columns (their S values were
+        // consumed above), so the dP^T columns are free as soon as they are read
+        tmem_st16(t_row + s_col + 16, wbuf);
+        // shared memory, 128-byte swizzle: [key row][64 queries]; this warp's
+        // queries are 16-byte chunks 4*half .. 4*half+3
+        uint8_t* ds_row = ds_rows + (it & 1) * L::kDSBytes;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int chunk = c2 * 4 + ch;  // 16-byte chunk = 8 queries
-            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
-                make_uint4(wbuf[ch * 4], wbuf[ch * 4 + 1], wbuf[ch * 4 + 2], wbuf[ch * 4 + 3]);
-          }
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = half * 4 + ch;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(wbuf[ch * 4], wbuf[ch * 4 + 1], wbuf[ch * 4 + 2], wbuf[ch * 4 + 3]);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(L::kBarDSReady));
+        mbar_arrive(bar(L::kBarDSReady + (it & 1)));
       }
     }
   } else {
     // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-    const int r = threadIdx.x - 128;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
-    const int wq = warp - 4;
+    const int r = threadIdx.x - 32 * kBwdDrainWarp0;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
+    const int wq = warp - kBwdDrainWarp0;
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
@@ -620,7 +694,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kBwdScoreWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -683,7 +757,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(320);
+      cfg.blockDim = dim3(kBwdThreads);
       cfg.dynamicSmemBytes = L::kAllocBytes;
       cfg.stream = stream;
       cudaLaunchAttribute attr[1];
@@ -694,7 +768,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       if (cudaLaunchKernelEx(&cfg, bwd_main<D>, tq, tk, tv, tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
-      bwd_main<D><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
+      bwd_main<D><<<grid, kBwdThreads, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
     }
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     record_timing(true, stream);
