@@ -30,7 +30,7 @@
 //                      bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
 //
-// bwd_main warp roles (480 threads):
+// bwd_main warp roles (512 threads):
 //   warps 0-7   P^T / dS^T: warp w serves key rows 32*(w%4).. (its TMEM lanes)
 //               and query columns 32*(w/4).. of the block, so each SM
 //               sub-partition runs two of them and one's latencies hide
@@ -38,24 +38,29 @@
 //   warps 8-11  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
 //   warp 12     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
 //               block into a 3-stage ring;
-//   warp 13     TMEM owner; one thread issues S^T and dP^T;
-//   warp 14     one thread issues dV, dK and dQ^T.
+//   warp 13     TMEM owner; one thread issues S^T;
+//   warp 14     one thread issues dP^T;
+//   warp 15     one thread issues dV, dK and dQ^T.
 // TMEM columns: S^T double buffer [0,64) [64,128); P^T and dS^T (bf16 pairs)
 // replace it in place: query columns 32h..32h+31 of S^T are read by the warps
 // of half h, which then write their 16 columns of P^T and 16 of dS^T over
 // them (P^T at 32h, dS^T at 32h+16), so the two halves never touch each
 // other's columns;
 // dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
-// Two issuing threads: a thread that has MMAs queued and then waits on a
+// Three issuing threads: a thread that has MMAs queued and then waits on a
 // barrier only continues once the tensor core has taken those MMAs, so a lone
-// issuer lets the tensor core run dry at every wait.  The score side (S^T as
-// soon as Q_i has landed and its S^T buffer is free, dP^T as soon as the
-// softmax warps have read the previous one) and the gradient side (dV, dK, dQ^T
-// as the softmax warps publish P^T and dS^T) wait on different events, and
-// each one's waits are covered by the MMAs the other has queued.  Buffers that
-// one side fills and the other reads are handed back through their own
-// barriers: an S^T buffer is free once dK of the block that used it is done,
-// a shared dS^T buffer once its dQ^T is done.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
+// issuer lets the tensor core run dry at every wait and delays its own view of
+// the next event.  S^T (as soon as Q_i has landed and its S^T buffer is free),
+// dP^T (as soon as the softmax warps have read the previous one: the one
+// loop-carried dependency of the block sequence, so its issuer has nothing else
+// queued) and the gradients (dV, dK, dQ^T as the softmax warps publish P^T and
+// dS^T) wait on different events, and each one's waits are covered by the MMAs
+// the others have queued.  An S^T buffer is handed back once dK of the block
+// that used it is done.  The shared dS^T ring has three buffers: the softmax
+// warps write buffer i%3 only after S^T(i) is complete, which the S^T issuer
+// started after dK(i-2), which the gradient issuer started after dQ^T(i-3), the
+// buffer's previous reader; the tensor core completes one thread's MMAs in
+// order, so no separate hand-back is needed.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
 // block twice; lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
@@ -70,8 +75,9 @@ constexpr int kQB = 64;  // query rows per backward block
 constexpr int kBwdSmxWarps = 8;     // warps 0-7: P^T / dS^T
 constexpr int kBwdDrainWarp0 = 8;   // warps 8-11: dQ drain, dK/dV epilogue
 constexpr int kBwdTmaWarp = 12;
-constexpr int kBwdScoreWarp = 13;   // TMEM owner, S^T / dP^T issuer
-constexpr int kBwdGradWarp = 14;    // dV / dK / dQ^T issuer
+constexpr int kBwdScoreWarp = 13;   // TMEM owner, S^T issuer
+constexpr int kBwdDPWarp = 14;      // dP^T issuer
+constexpr int kBwdGradWarp = 15;    // dV / dK / dQ^T issuer
 constexpr int kBwdThreads = 32 * (kBwdGradWarp + 1);
 constexpr int kBwdSmxThreads = 32 * kBwdSmxWarps;
 
@@ -128,11 +134,11 @@ struct BwdSmem {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVTileBytes;
   static constexpr int kOffStage = kOffV + kKVTileBytes;
-  // dS^T [key][64 queries], two buffers by block parity: block i+1's dS^T is
-  // written while the dQ^T MMA of block i may still be reading block i's
+  // dS^T [key][64 queries], a ring of three buffers (block i uses i % 3)
+  static constexpr int kDSBufs = 3;
   static constexpr int kOffDS = kOffStage + kStages * kStageBytes;
   static constexpr int kDSBytes = kTile * kQB * 2;
-  static constexpr int kOffBar = kOffDS + 2 * kDSBytes;
+  static constexpr int kOffBar = kOffDS + kDSBufs * kDSBytes;
   static constexpr int kBarKVFull = 0, kBarKVEmpty = 1;
   static constexpr int kBarQFull = 2;                // kStages
   static constexpr int kBarQEmpty = 2 + kStages;     // kStages
@@ -147,9 +153,8 @@ struct BwdSmem {
   static constexpr int kBarDKVFull = kBarDQEmpty + 1;
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
-  static constexpr int kBarDSFree = kBarSFree + 2;     // 2: shared dS^T buffer read by dQ^T
-  static constexpr int kBarDrain = kBarDSFree + 2;     // 2: one per issuer
-  static constexpr int kNumBars = kBarDrain + 2;
+  static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
+  static constexpr int kNumBars = kBarDrain + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarKVFull), 1);
-    mbar_init(bar(L::kBarKVEmpty), 2);  // both issuers commit
+    mbar_init(bar(L::kBarKVEmpty), 3);  // every issuer commits
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
       mbar_init(bar(L::kBarQEmpty + s), 1);
@@ -292,11 +297,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKVFull), 1);
     mbar_init(bar(L::kBarDKVEmpty), 128);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kBarSFree + s), 1);
-      mbar_init(bar(L::kBarDSFree + s), 1);
-      mbar_init(bar(L::kBarDrain + s), 1);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFree + s), 1);
+    for (int s = 0; s < 3; ++s) mbar_init(bar(L::kBarDrain + s), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -370,15 +372,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // is the second column block of K (D = 128) or, at D = 64, the first again.
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
       constexpr uint32_t kHi = sdesc_hi(1024);
-      const bool score_side = (warp == kBwdScoreWarp);
+      const int role = warp - kBwdScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
         const BwdUnit w = bwd_unit(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (score_side) {
-          // ---- S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, both operands K-major
+        if (role < 2) {
+          // ---- S^T(i) = K Q_i^T or dP^T(i) = V dO_i^T, both operands K-major
           const uint32_t k_lo = sdesc_lo(sbase + L::kOffK, 16);
           const uint32_t v_lo = sdesc_lo(sbase + L::kOffV, 16);
           auto issue_kmajor = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
@@ -399,24 +401,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               ok = false;
               break;
             }
-            // the S^T buffer of block it-2 is free once its dV and dK are done
-            if (it >= 2 && !mbar_wait(bar(L::kBarSFree + (it & 1)), ((it >> 1) - 1) & 1,
-                                      abort_flag)) {
-              ok = false;
-              break;
+            if (role == 0) {
+              // the S^T buffer of block it-2 is free once its dV and dK are done
+              if (it >= 2 && !mbar_wait(bar(L::kBarSFree + (it & 1)), ((it >> 1) - 1) & 1,
+                                        abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_kmajor(tmem + L::kColS + (it & 1) * kQB, k_lo, sdesc_lo(q_base, 16));
+              umma_commit(bar(L::kBarSFull + (it & 1)));
+            } else {
+              // the dP^T columns are free once the softmax warps have read dP^T(it-1)
+              if (it >= 1 && !mbar_wait(bar(L::kBarDSReady + ((it - 1) & 1)),
+                                        ((it - 1) >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_kmajor(tmem + L::kColDP, v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
+              umma_commit(bar(L::kBarDPFull));
             }
-            tc_fence_after();
-            issue_kmajor(tmem + L::kColS + (it & 1) * kQB, k_lo, sdesc_lo(q_base, 16));
-            umma_commit(bar(L::kBarSFull + (it & 1)));
-            // the dP^T columns are free once the softmax warps have read dP^T(it-1)
-            if (it >= 1 && !mbar_wait(bar(L::kBarDSReady + ((it - 1) & 1)), ((it - 1) >> 1) & 1,
-                                      abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_kmajor(tmem + L::kColDP, v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
-            umma_commit(bar(L::kBarDPFull));
           }
           // K and V may be replaced once both sides are done with them
           if (ok) umma_commit(bar(L::kBarKVEmpty));
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t dsb_lo = ds_lo + (((it & 1) * L::kDSBytes) >> 4);
+            const uint32_t dsb_lo = ds_lo + (((it % L::kDSBufs) * L::kDSBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint32_t ko = (kk * 16 * 128) >> 4;
@@ -479,7 +484,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 umma_ss_w<1>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
             }
             umma_commit(bar(L::kBarDQFull));
-            umma_commit(bar(L::kBarDSFree + (it & 1)));
           }
           if (ok) {
             umma_commit(bar(L::kBarKVEmpty));
@@ -487,8 +491,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      umma_commit(bar(L::kBarDrain + (score_side ? 0 : 1)));
-      drain_wait_b(bar(L::kBarDrain + (score_side ? 0 : 1)), 0);
+      umma_commit(bar(L::kBarDrain + role));
+      drain_wait_b(bar(L::kBarDrain + role), 0);
     }
   } else if (warp < kBwdSmxWarps) {
     // ------------------------------------------------------------ P^T / dS^T
@@ -556,12 +560,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dl[4 * q] = x.x, dl[4 * q + 1] = x.y, dl[4 * q + 2] = x.z, dl[4 * q + 3] = x.w;
         }
         if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
-        // the shared dS^T buffer of this block was last read by dQ^T(it-2)
-        if (it >= 2 &&
-            !warp_wait_b(bar(L::kBarDSFree + (it & 1)), ((it >> 1) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
         uint32_t wbuf[16];
         {
@@ -579,7 +577,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st16(t_row + s_col + 16, wbuf);
         // shared memory, 128-byte swizzle: [key row][64 queries]; this warp's
         // queries are 16-byte chunks 4*half .. 4*half+3
-        uint8_t* ds_row = ds_rows + (it & 1) * L::kDSBytes;
+        uint8_t* ds_row = ds_rows + (it % L::kDSBufs) * L::kDSBytes;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int chunk = half * 4 + ch;
