@@ -165,7 +165,8 @@ def bwd_status(workspace: torch.Tensor, stream=None) -> int:
 
 
 def exp2_test(x: torch.Tensor, which: int, stream=None) -> torch.Tensor:
-    """2^x through the kernel's MUFU path (which=0) or polynomial path (which=1)."""
+    """2^x through the kernel's MUFU path (which=0), polynomial path (which=1) or
+    packed two-lane polynomial path (which=2)."""
     if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
         raise TypeError("x must be a contiguous fp32 CUDA tensor")
     y = torch.empty_like(x)

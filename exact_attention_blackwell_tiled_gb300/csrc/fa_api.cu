@@ -275,7 +275,7 @@ int fa_bwd_status(const void* workspace, fa_stream_t stream) {
 
 int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream) {
   t_launches = 0;
-  if (n < 0 || (which != 0 && which != 1)) return FA_ERR_INVALID_ARG;
+  if (n < 0 || which < 0 || which > 2) return FA_ERR_INVALID_ARG;
   if (n > 0 && (!x || !y)) return FA_ERR_INVALID_ARG;
   if (n == 0) return FA_OK;
   int rc = check_device();

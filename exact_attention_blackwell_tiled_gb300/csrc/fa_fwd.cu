@@ -67,6 +67,11 @@ struct FwdLayout {
   static constexpr int kAllocBytes = kBytes + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
+  // Exponential split (FlashAttention-4 pages, key contribution #2): of every 8
+  // column pairs of a score row, kPolyPairs go through the cubic on the FMA
+  // pipe (two lanes per packed instruction) and the rest through MUFU ex2.
+  // Chosen by measurement on GB300, whose MUFU rate is twice B200's.
+  static constexpr int kPolyPairs = (D == 64) ? 1 : 0;
 };
 
 // The r-th unit this CTA processes (-1 when it has no more).  Every role of
@@ -399,7 +404,13 @@ __global__ void __launch_bounds__(320, 1)
               const uint32_t* src = (i < 16) ? w0 : w1;
               const int e = (i & 15) * 2;
               const float2 tt = __ffma2_rn(make_float2(u2f(src[e]), u2f(src[e + 1])), c2, nm2);
-              const float p0 = ex2_mufu(tt.x), p1 = ex2_mufu(tt.y);
+              float p0, p1;
+              if ((i & 7) < L::kPolyPairs) {
+                const float2 pp = ex2_poly2(tt);
+                p0 = pp.x, p1 = pp.y;
+              } else {
+                p0 = ex2_mufu(tt.x), p1 = ex2_mufu(tt.y);
+              }
               sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
             }
@@ -577,7 +588,13 @@ __global__ void exp2_test_kernel(const float* __restrict__ x, float* __restrict_
                                  int which) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = which ? ex2_poly(x[i]) : ex2_mufu(x[i]);
+  {
+    const float xi = x[i];
+    if (which == 2)  // packed path: even elements through lane 0, odd through lane 1
+      y[i] = (i & 1) ? ex2_poly2(make_float2(0.0f, xi)).y : ex2_poly2(make_float2(xi, 0.0f)).x;
+    else
+      y[i] = which ? ex2_poly(xi) : ex2_mufu(xi);
+  }
 }
 
 int launch_exp2_test(const float* x, float* y, int64_t n, int which, cudaStream_t stream) {

@@ -115,7 +115,9 @@ const char* fa_status_string(int status);
  * Test hook for the exponential split of the forward softmax (FlashAttention-4
  * pages, key contribution #2: a degree-3 polynomial on the FMA units run beside
  * the MUFU exp2).  Writes y[i] = 2^x[i] computed the way the kernel does:
- * which = 0 the hardware ex2.approx path, which = 1 the polynomial path.
+ * which = 0 the hardware ex2.approx path, which = 1 the polynomial path,
+ * which = 2 the same polynomial on the packed two-lane fp32 pipe (the form the
+ * forward softmax runs; even elements go through lane 0, odd through lane 1).
  * x, y: device fp32 arrays of n elements.  Inputs below -125 give 2^-125 on the
  * polynomial path (the kernel's clamp), values above 64 are not supported.
  */

@@ -102,7 +102,8 @@ def test_workspace_size(L):
 def test_exp2_hook_validation(L):
     assert L.fa_exp2_test(None, None, 0, 0, None) == 0
     assert L.fa_exp2_test(None, None, -1, 0, None) == 1
-    assert L.fa_exp2_test(P16, P16, 4, 2, None) == 1
+    assert L.fa_exp2_test(P16, P16, 4, 3, None) == 1
+    assert L.fa_exp2_test(P16, P16, 4, -1, None) == 1
 
 
 def test_python_binding_refuses_cpu_tensors():

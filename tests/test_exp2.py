@@ -27,7 +27,8 @@ def _inputs():
     return torch.cat([dense, rnd, edges]).float()
 
 
-@pytest.mark.parametrize("which,bound", [(0, 2.0 ** -20), (1, 1.2e-4)], ids=["mufu", "poly"])
+@pytest.mark.parametrize("which,bound", [(0, 2.0 ** -20), (1, 1.2e-4), (2, 1.2e-4)],
+                         ids=["mufu", "poly", "poly_packed"])
 def test_exp2_relative_error(which, bound):
     x = _inputs()
     y = fa.exp2_test(x.cuda(), which).cpu().double().numpy()
@@ -40,8 +41,9 @@ def test_exp2_relative_error(which, bound):
 
 def test_exp2_poly_masked_inputs():
     x = torch.tensor([-float("inf"), -1e30, -200.0, -126.0], device="cuda")
-    y = fa.exp2_test(x, 1).cpu()
-    assert bool((y >= 0).all()) and bool((y <= 2.0 ** -124).all())
+    for which in (1, 2):
+        y = fa.exp2_test(x, which).cpu()
+        assert bool((y >= 0).all()) and bool((y <= 2.0 ** -124).all())
     y0 = fa.exp2_test(x, 0).cpu()
     assert bool((y0 >= 0).all()) and bool((y0 <= 2.0 ** -126).all())
     assert bool((y0[:3] == 0).all())  # below the normal range the hardware path flushes to 0
