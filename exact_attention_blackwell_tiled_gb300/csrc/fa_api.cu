@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -49,6 +50,10 @@ int check_shape(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
   const long long bh = (long long)B * Hq;
   if (bh > (1LL << 30) || (long long)Sq > (1LL << 30) || (long long)Sk > (1LL << 30))
     return FA_ERR_INVALID_ARG;
+  // Row indices over all heads (q rows padded to 128) are 32-bit in the kernels.
+  const long long q_rows = bh * (((long long)Sq + 127) / 128 * 128);
+  const long long kv_rows = (long long)B * Hkv * Sk;
+  if (q_rows > INT32_MAX || kv_rows > INT32_MAX) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 

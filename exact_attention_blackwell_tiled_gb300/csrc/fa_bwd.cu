@@ -78,40 +78,74 @@ constexpr int kBwdTmaWarp = 12;
 constexpr int kBwdScoreWarp = 13;   // TMEM owner, S^T issuer
 constexpr int kBwdDPWarp = 14;      // dP^T issuer
 constexpr int kBwdGradWarp = 15;    // dV / dK / dQ^T issuer
+static_assert(kBwdDPWarp == kBwdScoreWarp + 1 && kBwdGradWarp == kBwdScoreWarp + 2,
+              "the issuers' role is warp - kBwdScoreWarp");
 constexpr int kBwdThreads = 32 * (kBwdGradWarp + 1);
 constexpr int kBwdSmxThreads = 32 * kBwdSmxWarps;
 
 // ------------------------------------------------------------------ preprocess
 
+// Each lane owns 8 consecutive elements (16 bytes) of a row, so a row takes D/8
+// lanes and a warp covers 32/(D/8) rows per step; a warp works on kPreUnroll
+// steps at once to keep several 16-byte loads in flight.  Row indices over all
+// heads are 32-bit (the host bounds them).
+constexpr int kPreUnroll = 4;
+
 template <int D>
-__global__ void bwd_preprocess(const BwdArgs a) {
-  // one warp per (b, h, padded row)
-  const int warps_per_block = blockDim.x / 32;
-  const long long total_rows = (long long)a.B * a.Hq * a.Sq_pad;
+__global__ void __launch_bounds__(256) bwd_preprocess(const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerStep = 32 / kLanesPerRow;
+  constexpr int kRowsPerWarp = kRowsPerStep * kPreUnroll;
+  const uint32_t total_rows = (uint32_t)a.B * a.Hq * a.Sq_pad;
   const int lane = threadIdx.x & 31;
-  const long long gwarp = (long long)blockIdx.x * warps_per_block + (threadIdx.x >> 5);
-  const long long nwarps = (long long)gridDim.x * warps_per_block;
-  constexpr int kPer = D / 32;  // elements per lane
-  for (long long r = gwarp; r < total_rows; r += nwarps) {
-    const long long bh = r / a.Sq_pad;
-    const int i = (int)(r - bh * a.Sq_pad);
-    float acc = 0.f;
-    if (i < a.Sq) {
-      const size_t off = ((size_t)bh * a.Sq + i) * D + lane * kPer;
-      const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(a.o) + off;
-      const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(a.dO) + off;
+  const int sub = lane / kLanesPerRow, seg = lane % kLanesPerRow;
+  const uint32_t warps_per_block = blockDim.x / 32;
+  const uint32_t nwarps = gridDim.x * warps_per_block;
+  for (uint32_t g = blockIdx.x * warps_per_block + (threadIdx.x >> 5);
+       (uint64_t)g * kRowsPerWarp < total_rows; g += nwarps) {
+    uint4 ov[kPreUnroll], gv[kPreUnroll];
+    bool real[kPreUnroll];
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) acc += __bfloat162float(o[e]) * __bfloat162float(g[e]);
+    for (int u = 0; u < kPreUnroll; ++u) {
+      const uint32_t r = g * kRowsPerWarp + u * kRowsPerStep + sub;
+      const uint32_t bh = r / (uint32_t)a.Sq_pad;
+      const uint32_t i = r - bh * (uint32_t)a.Sq_pad;
+      real[u] = r < total_rows && i < (uint32_t)a.Sq;
+      ov[u] = gv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (real[u]) {
+        const size_t off = ((size_t)bh * a.Sq + i) * D + seg * 8;
+        ov[u] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + off);
+        gv[u] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + off);
+      }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
-      a.delta[r] = acc;
-      a.lse2[r] = (i < a.Sq) ? a.lse[bh * a.Sq + i] * 1.4426950408889634f : INFINITY;
-    }
-    float* dqa = a.dq_acc + (size_t)r * D + lane * kPer;
+    for (int u = 0; u < kPreUnroll; ++u) {
+      const uint32_t r = g * kRowsPerWarp + u * kRowsPerStep + sub;
+      const uint32_t* ow = &ov[u].x;
+      const uint32_t* gw = &gv[u].x;
+      float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) dqa[e] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+#pragma unroll
+      for (int sft = kLanesPerRow / 2; sft > 0; sft >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+      if (r < total_rows) {
+        if (seg == 0) {
+          const uint32_t bh = r / (uint32_t)a.Sq_pad;
+          const uint32_t i = r - bh * (uint32_t)a.Sq_pad;
+          a.delta[r] = acc;
+          a.lse2[r] = real[u] ? a.lse[(size_t)bh * a.Sq + i] * 1.4426950408889634f : INFINITY;
+        }
+        float4* dqa = reinterpret_cast<float4*>(a.dq_acc + (size_t)r * D + seg * 8);
+        dqa[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dqa[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
   const long long nsem = (long long)a.B * a.Hq * a.n_qblk;
   for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < nsem;
@@ -702,15 +736,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ------------------------------------------------------------------ dQ convert
 
 template <int D>
-__global__ void bwd_dq_convert(const BwdArgs a) {
-  // 8 elements per thread
-  const long long total = (long long)a.B * a.Hq * a.Sq * (D / 8);
-  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
-       x += (long long)gridDim.x * blockDim.x) {
-    const long long row = x / (D / 8);
-    const int c8 = (int)(x - row * (D / 8));
-    const long long bh = row / a.Sq;
-    const int i = (int)(row - bh * a.Sq);
+__global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
+  // 8 elements (two 16-byte loads, one 16-byte store) per thread; row indices
+  // over all heads are 32-bit (the host bounds them)
+  constexpr uint32_t kPerRow = D / 8;
+  const uint64_t total = (uint64_t)a.B * a.Hq * a.Sq * kPerRow;
+  for (uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t row = (uint32_t)(x / kPerRow);
+    const uint32_t c8 = (uint32_t)(x - (uint64_t)row * kPerRow);
+    const uint32_t bh = row / (uint32_t)a.Sq;
+    const uint32_t i = row - bh * (uint32_t)a.Sq;
     const float4* src =
         reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Sq_pad + i) * D + c8 * 8);
     const float4 x0 = src[0], x1 = src[1];
@@ -741,7 +777,8 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // 1. preprocess
   {
     const long long rows = (long long)a.B * a.Hq * a.Sq_pad;
-    long long blocks = (rows + 7) / 8;  // 8 warps per block
+    constexpr long long kRowsPerBlock = 8LL * (32 / (D / 8)) * kPreUnroll;  // 8 warps
+    long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks > 8LL * sms) blocks = 8LL * sms;
     if (blocks < 1) blocks = 1;
     bwd_preprocess<D><<<(int)blocks, 256, 0, stream>>>(a);

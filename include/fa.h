@@ -44,7 +44,9 @@ extern "C" {
 
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0, non-finite scale */
+  FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0, non-finite scale,
+                             or more than 2^31 - 1 rows over all heads (B * Hq * Sq with Sq
+                             rounded up to 128, or B * Hkv * Sk) */
   FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 / 128, or a device that is not sm_103 */
   FA_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned (TMA requirement) */
   FA_ERR_WORKSPACE = 4,   /* backward workspace missing, misaligned or too small */
@@ -60,7 +62,7 @@ typedef void* fa_stream_t;
  *   q   [B, Hq,  Sq, D] bf16      k, v [B, Hkv, Sk, D] bf16
  *   o   [B, Hq,  Sq, D] bf16 out  lse  [B, Hq, Sq] fp32 out (natural log)
  * Sizes: B, Hq, Hkv, Sk >= 1; Sq >= 0 (Sq == 0 is a no-op); D in {64, 128};
- * scale finite.  causal != 0 applies the top-left mask q_idx >= kv_idx, which
+ * B * Hq * Sq (Sq rounded up to 128) and B * Hkv * Sk below 2^31; scale finite.  causal != 0 applies the top-left mask q_idx >= kv_idx, which
  * leaves no row empty when Sk >= 1.  Pointers must be non-null and 16-byte
  * aligned (when Sq == 0 nothing is checked, read or written).  Output rows are
  * written exactly once; nothing outside them is touched.

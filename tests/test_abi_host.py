@@ -99,6 +99,14 @@ def test_workspace_size(L):
     assert big % 256 == 0
 
 
+def test_row_count_limit(L):
+    # rows over all heads are 32-bit in the kernels: B * Hq * ceil128(Sq) < 2^31
+    assert L.fa_bwd_workspace_bytes(1 << 14, 1, 1, 1 << 17, 128, 64, 0) == 0
+    assert L.fa_bwd_workspace_bytes(1, 1, 1, 128, 1 << 17, 64, 0) > 0
+    assert L.fa_fwd(P16, P16, P16, P16, P16, 4, 1, 1, 128, 1 << 30, 64, 0, 1.0, None) == 1
+    assert L.fa_fwd(P16, P16, P16, P16, P16, 1 << 13, 2, 1, 1 << 17, 128, 64, 0, 1.0, None) == 1
+
+
 def test_exp2_hook_validation(L):
     assert L.fa_exp2_test(None, None, 0, 0, None) == 0
     assert L.fa_exp2_test(None, None, -1, 0, None) == 1
