@@ -234,6 +234,26 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
   }
 }
 
+// 4x4 transpose of 32-bit values within the lane group (lane & ~3) .. +3: on
+// return v[m] holds what lane (lane & ~3) + m held in v[lane & 3].
+__device__ __forceinline__ void xpose4(uint32_t (&v)[4], int lane) {
+#pragma unroll
+  for (int mask = 1; mask < 4; mask <<= 1) {
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s & mask) continue;
+      const int s2 = s | mask;
+      const uint32_t send = upper ? v[s] : v[s2];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, mask);
+      if (upper)
+        v[s] = recv;
+      else
+        v[s2] = recv;
+    }
+  }
+}
+
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -357,9 +377,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit(a, u, group);
-        if (!mbar_wait(bar(L::kBarKVEmpty), (unit & 1) ^ 1, abort_flag)) { ok = false; break; }
+      // K_j and V_j of a unit, once every issuer is done with the previous ones
+      auto load_kv = [&](const BwdUnit& w, uint32_t un) -> bool {
+        if (!mbar_wait(bar(L::kBarKVEmpty), (un & 1) ^ 1, abort_flag)) return false;
         mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVTileBytes);
 #pragma unroll
         for (int cb = 0; cb < L::kColBlocks; ++cb) {
@@ -368,7 +388,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sbase + L::kOffV + cb * L::kKVBlockBytes, &tm_v, bar(L::kBarKVFull),
                       cb * 64, w.j * kTile, w.bhk);
         }
+        return true;
+      };
+      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
+        const BwdUnit w = bwd_unit(a, u, group);
+        // The unit's first blocks' Q / dO go out before its K / V: their stages
+        // free up while the previous unit still holds K and V, so they have
+        // landed by the time K and V can be replaced.
+        const int early = w.n_it < L::kStages ? w.n_it : L::kStages;
         for (int t = 0; t < w.n_it; ++t, ++it) {
+          if (t == early) {
+            if (!load_kv(w, unit)) { ok = false; break; }
+          }
           const int gi = t / w.n_blk;
           const int iq = w.lo + (t - gi * w.n_blk);
           const int bh = w.b * a.Hq + w.hk * group + gi;
@@ -391,6 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           bulk_load(sdst + 2 * L::kQTileBytes + kQB * 4, a.delta + voff, kQB * 4,
                     bar(L::kBarQFull + st));
         }
+        if (ok && early == w.n_it && !load_kv(w, unit)) ok = false;
       }
       if (unit > 0) drain_wait_b(bar(L::kBarKVFull), (unit - 1) & 1);
       for (uint32_t n = (it > (uint32_t)L::kStages ? it - L::kStages : 0); n < it; ++n)
@@ -687,11 +719,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = group_all(warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag), 2);
       if (!ok) break;
       tc_fence_after();
-      const int kv = w.j * kTile + r;
-      const bool row_ok = kv < a.Sk;
-      const size_t out_off = ((size_t)w.bhk * a.Sk + (row_ok ? kv : 0)) * D;
-      __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(a.dk) + out_off;
-      __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(a.dv) + out_off;
+      // Each thread holds one key row; to store whole 64-byte row pieces per
+      // warp instruction, the four lanes of a group trade 16-byte pieces (a 4x4
+      // transpose) so that lane 4k+i writes piece i of rows 4k..4k+3.
+      const int grp = lane & ~3, pc = lane & 3;
+      const int row0 = w.j * kTile + wq * 32 + grp;  // first key row of the lane group
+      __nv_bfloat16* dk_base = reinterpret_cast<__nv_bfloat16*>(a.dk) + (size_t)w.bhk * a.Sk * D;
+      __nv_bfloat16* dv_base = reinterpret_cast<__nv_bfloat16*>(a.dv) + (size_t)w.bhk * a.Sk * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t vk[32], vv[32];
@@ -703,24 +737,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) vk[e] = vv[e] = 0u;
         }
-        if (row_ok) {
-          uint32_t wk[16], wv[16];
+        if (c == D / 32 - 1) {
+          // every TMEM read of dK / dV is done: the accumulators are free
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDKVEmpty));
+        }
+        uint32_t wk[16], wv[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            wk[e] = pack_bf16x2(u2f(vk[2 * e]) * a.scale, u2f(vk[2 * e + 1]) * a.scale);
-            wv[e] = pack_bf16x2(u2f(vv[2 * e]), u2f(vv[2 * e + 1]));
-          }
-          uint4* dk4 = reinterpret_cast<uint4*>(dk_row + c * 32);
-          uint4* dv4 = reinterpret_cast<uint4*>(dv_row + c * 32);
+        for (int e = 0; e < 16; ++e) {
+          wk[e] = pack_bf16x2(u2f(vk[2 * e]) * a.scale, u2f(vk[2 * e + 1]) * a.scale);
+          wv[e] = pack_bf16x2(u2f(vv[2 * e]), u2f(vv[2 * e + 1]));
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dk4[e] = make_uint4(wk[4 * e], wk[4 * e + 1], wk[4 * e + 2], wk[4 * e + 3]);
-            dv4[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+        for (int wd = 0; wd < 4; ++wd) {  // word wd of each 16-byte piece
+          uint32_t xk[4] = {wk[wd], wk[4 + wd], wk[8 + wd], wk[12 + wd]};
+          uint32_t xv[4] = {wv[wd], wv[4 + wd], wv[8 + wd], wv[12 + wd]};
+          xpose4(xk, lane);
+          xpose4(xv, lane);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) wk[4 * m + wd] = xk[m], wv[4 * m + wd] = xv[m];
+        }
+        // wk[4m..4m+3] is now piece pc of row row0 + m
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          if (row0 + m < a.Sk) {
+            const size_t off = (size_t)(row0 + m) * D + c * 32 + pc * 8;
+            *reinterpret_cast<uint4*>(dk_base + off) =
+                make_uint4(wk[4 * m], wk[4 * m + 1], wk[4 * m + 2], wk[4 * m + 3]);
+            *reinterpret_cast<uint4*>(dv_base + off) =
+                make_uint4(wv[4 * m], wv[4 * m + 1], wv[4 * m + 2], wv[4 * m + 3]);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDKVEmpty));
     }
   }
 
