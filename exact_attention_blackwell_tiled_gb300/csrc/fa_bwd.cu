@@ -392,10 +392,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
         const BwdUnit w = bwd_unit(a, u, group);
-        // The unit's first blocks' Q / dO go out before its K / V: their stages
-        // free up while the previous unit still holds K and V, so they have
-        // landed by the time K and V can be replaced.
-        const int early = w.n_it < L::kStages ? w.n_it : L::kStages;
+        // The unit's first block's Q / dO go out before its K / V: its stage
+        // frees up while the previous unit still holds K and V, so it has landed
+        // by the time K and V can be replaced.  Later blocks follow K and V, which
+        // the first S^T needs as much as Q.
+        const int early = w.n_it < 1 ? w.n_it : 1;
         for (int t = 0; t < w.n_it; ++t, ++it) {
           if (t == early) {
             if (!load_kv(w, unit)) { ok = false; break; }
