@@ -37,6 +37,14 @@ def _bind(lib):
     lib.oracle_bwd_units.argtypes = [p, p, p, p, i, i, i, i, i, i, i, d, p, ctypes.c_int64,
                                      p, p, p, p, p]
     lib.oracle_bwd_units.restype = i
+    lib.oracle_fwd_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, p]
+    lib.oracle_fwd_mod.restype = i
+    lib.oracle_fwd_rows_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, ctypes.c_int64,
+                                        p, p]
+    lib.oracle_fwd_rows_mod.restype = i
+    lib.oracle_bwd_units_mod.argtypes = [p, p, p, p, i, i, i, i, i, i, d, i, i, p, p,
+                                         ctypes.c_int64, p, p, p, p, p]
+    lib.oracle_bwd_units_mod.restype = i
     for name in ("oracle_tiled_fwd_f64", "oracle_tiled_fwd_f32"):
         f = getattr(lib, name)
         f.argtypes = [p, p, p, i, i, i, i, i, i, i, d, i, i, i, d, p, p, p, p]
@@ -130,6 +138,76 @@ def bwd(q, k, v, do, causal: bool, scale: float, units=None, lib=None):
                               _ptr(dk), _ptr(dv), _ptr(o), _ptr(lse))
     if rc:
         raise ValueError(f"oracle_bwd_units rejected its arguments ({rc})")
+    return dq, dk, dv, o, lse
+
+
+def _slopes(slopes, Hq):
+    if slopes is None:
+        return None
+    a = _f64(slopes).reshape(-1)
+    assert a.shape == (Hq,), "one slope per query head"
+    return a
+
+
+def fwd_mod(q, k, v, scale: float, window_left: int = -1, window_right: int = -1, slopes=None,
+            lib=None):
+    """Forward with the score modification: key j visible to query i iff
+    (window_left < 0 or j >= i - window_left) and (window_right < 0 or
+    j <= i + window_right); score scale*q.k + slopes[h]*(j - i).  Returns (O, LSE)."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
+    sl = _slopes(slopes, Hq)
+    o = np.zeros((B, Hq, Sq, D))
+    lse = np.zeros((B, Hq, Sq))
+    rc = lib.oracle_fwd_mod(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
+                            int(window_left), int(window_right),
+                            None if sl is None else _ptr(sl), _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_fwd_mod rejected its arguments ({rc})")
+    return o, lse
+
+
+def fwd_rows_mod(q, k, v, scale: float, rows, window_left: int = -1, window_right: int = -1,
+                 slopes=None, lib=None):
+    """fwd_mod for selected flat rows (b*Hq + h)*Sq + i. Returns (O [n,D], LSE [n])."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
+    sl = _slopes(slopes, Hq)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    o = np.zeros((len(rows), D))
+    lse = np.zeros(len(rows))
+    rc = lib.oracle_fwd_rows_mod(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
+                                 int(window_left), int(window_right),
+                                 None if sl is None else _ptr(sl), _ptr(rows), len(rows),
+                                 _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_fwd_rows_mod rejected its arguments ({rc})")
+    return o, lse
+
+
+def bwd_mod(q, k, v, do, scale: float, window_left: int = -1, window_right: int = -1,
+            slopes=None, units=None, lib=None):
+    """Backward with the score modification (see fwd_mod); same return as bwd."""
+    lib = lib or load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
+    sl = _slopes(slopes, Hq)
+    if units is None:
+        units = np.arange(B * Hkv)
+    units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    o = np.full(q.shape, np.nan)
+    lse = np.full((B, Hq, Sq), np.nan)
+    rc = lib.oracle_bwd_units_mod(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Sq, Sk, D,
+                                  float(scale), int(window_left), int(window_right),
+                                  None if sl is None else _ptr(sl), _ptr(units), len(units),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_bwd_units_mod rejected its arguments ({rc})")
     return dq, dk, dv, o, lse
 
 

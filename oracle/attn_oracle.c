@@ -276,3 +276,189 @@ int oracle_bwd_units(const double* q, const double* k, const double* v, const do
 #define LOG2 log2f
 #define TILED_NAME oracle_tiled_fwd_f32
 #include "tiled_body.h"
+
+/* ---- score modification: a sliding window and a linear relative-position bias ----
+ *
+ * The pages name score modifications, relative position biases and custom masks
+ * (FlexAttention integration) without defining any.  Reading taken: key j is
+ * visible to query i iff (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr), so
+ * wl = -1, wr = 0 is the causal mask and wl = wr = -1 no mask; the score of a
+ * visible pair in query head h is scale * q_i . k_j + slope[h] * (j - i) (slopes
+ * NULL: no bias).  The row's softmax, LSE and the gradients follow the plain
+ * definition with that score.
+ */
+
+/* Visible keys of query i: the interval [*lo, *hi) (empty when *hi <= *lo). */
+static void mod_key_range(long i, long Sk, int wl, int wr, long* lo, long* hi) {
+  long a = 0, b = Sk;
+  if (wl >= 0 && i - wl > a) a = i - wl;
+  if (wr >= 0 && i + wr + 1 < b) b = i + wr + 1;
+  *lo = a;
+  *hi = (b > a) ? b : a;
+}
+
+/* Score of (i, j) with the bias. */
+static double mod_score(const double* qi, const double* kj, long D, double scale, double slope,
+                        long i, long j) {
+  return scale * dot(qi, kj, D) + slope * (double)(j - i);
+}
+
+/* One query row: O (D values) and LSE over the visible keys; s is scratch [Sk]. */
+static void mod_fwd_row(const double* qi, const double* k_head, const double* v_head, long D,
+                        long i, long lo, long hi, double scale, double slope, double* s,
+                        double* oi, double* lse_out) {
+  for (long d = 0; d < D; ++d) oi[d] = 0.0;
+  if (hi <= lo) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  double top = -INFINITY;
+  for (long j = lo; j < hi; ++j) {
+    s[j] = mod_score(qi, k_head + j * D, D, scale, slope, i, j);
+    top = fmax(top, s[j]);
+  }
+  double z = 0.0;
+  for (long j = lo; j < hi; ++j) z += exp(s[j] - top);
+  const double row_lse = top + log(z);
+  for (long j = lo; j < hi; ++j) {
+    const double w = exp(s[j] - row_lse);
+    for (long d = 0; d < D; ++d) oi[d] += w * v_head[j * D + d];
+  }
+  *lse_out = row_lse;
+}
+
+static double head_slope(const double* slopes, long h) { return slopes ? slopes[h] : 0.0; }
+
+/* Full forward with the score modification: O [B,Hq,Sq,D], LSE [B,Hq,Sq]. */
+int oracle_fwd_mod(const double* q, const double* k, const double* v, int B, int Hq, int Hkv,
+                   int Sq, int Sk, int D, double scale, int wl, int wr, const double* slopes,
+                   double* o, double* lse) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  const long total = (long)B * Hq * Sq;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (long flat = 0; flat < total; ++flat) {
+      const long i = flat % Sq, bh = flat / Sq;
+      const long b = bh / Hq, h = bh % Hq;
+      const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
+      long lo, hi;
+      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,
+                  scale, head_slope(slopes, h), s, o + flat * D, lse + flat);
+    }
+    free(s);
+  }
+  return 0;
+}
+
+/* Forward with the score modification for selected flat rows (b*Hq + h)*Sq + i. */
+int oracle_fwd_rows_mod(const double* q, const double* k, const double* v, int B, int Hq,
+                        int Hkv, int Sq, int Sk, int D, double scale, int wl, int wr,
+                        const double* slopes, const int64_t* rows, int64_t n_rows,
+                        double* o_rows, double* lse_rows) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  const long total = (long)B * Hq * Sq;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= total) return -3;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n_rows; ++r) {
+      const long flat = (long)rows[r];
+      const long i = flat % Sq, bh = flat / Sq;
+      const long b = bh / Hq, h = bh % Hq;
+      const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
+      long lo, hi;
+      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,
+                  scale, head_slope(slopes, h), s, o_rows + r * D, lse_rows + r);
+    }
+    free(s);
+  }
+  return 0;
+}
+
+/*
+ * Backward with the score modification for kv-head units u = b*Hkv + hk: dK, dV
+ * of the unit and dQ, O, LSE of its group's q heads.  The bias does not depend
+ * on q or k, so it enters the gradients only through P.
+ */
+int oracle_bwd_units_mod(const double* q, const double* k, const double* v, const double* dO,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale, int wl,
+                         int wr, const double* slopes, const int64_t* units, int64_t n_units,
+                         double* dq, double* dk, double* dv, double* o, double* lse) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  for (int64_t u = 0; u < n_units; ++u)
+    if (units[u] < 0 || units[u] >= (int64_t)B * Hkv) return -3;
+  const int g = Hq / Hkv;
+  double* dsum = (double*)malloc(sizeof(double) * (size_t)(Sq > 0 ? Sq : 1) * (size_t)g);
+  if (!dsum) return -4;
+  for (int64_t u = 0; u < n_units; ++u) {
+    const long b = (long)(units[u] / Hkv), hk = (long)(units[u] % Hkv);
+    const long kvh = b * Hkv + hk;
+    const double* kh = k + kvh * (long)Sk * D;
+    const double* vh = v + kvh * (long)Sk * D;
+    /* per query row of the group: O, LSE, the row term sum_d dO O, and dQ */
+    for (int gi = 0; gi < g; ++gi) {
+      const long h = hk * g + gi;
+      const long row0 = (b * Hq + h) * (long)Sq;
+      const double slope = head_slope(slopes, h);
+#pragma omp parallel
+      {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long i = 0; i < Sq; ++i) {
+          long lo, hi;
+          mod_key_range(i, Sk, wl, wr, &lo, &hi);
+          const double* qi = q + (row0 + i) * D;
+          const double* gi_row = dO + (row0 + i) * D;
+          double* oi = o + (row0 + i) * D;
+          double* dqi = dq + (row0 + i) * D;
+          mod_fwd_row(qi, kh, vh, D, i, lo, hi, scale, slope, s, oi, lse + row0 + i);
+          const double rterm = dot(gi_row, oi, D);
+          dsum[gi * (long)Sq + i] = rterm;
+          for (long d = 0; d < D; ++d) dqi[d] = 0.0;
+          for (long j = lo; j < hi; ++j) {
+            const double w = exp(s[j] - lse[row0 + i]);
+            const double g_w = w * (dot(gi_row, vh + j * D, D) - rterm);
+            for (long d = 0; d < D; ++d) dqi[d] += scale * g_w * kh[j * D + d];
+          }
+        }
+        free(s);
+      }
+    }
+    /* per key row: dK_j, dV_j over the queries that see key j */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long j = 0; j < Sk; ++j) {
+      double* dkj = dk + (kvh * (long)Sk + j) * D;
+      double* dvj = dv + (kvh * (long)Sk + j) * D;
+      for (long d = 0; d < D; ++d) dkj[d] = dvj[d] = 0.0;
+      for (int gi = 0; gi < g; ++gi) {
+        const long h = hk * g + gi;
+        const long row0 = (b * Hq + h) * (long)Sq;
+        const double slope = head_slope(slopes, h);
+        for (long i = 0; i < Sq; ++i) {
+          long lo, hi;
+          mod_key_range(i, Sk, wl, wr, &lo, &hi);
+          if (j < lo || j >= hi) continue;
+          const double* qi = q + (row0 + i) * D;
+          const double* gi_row = dO + (row0 + i) * D;
+          const double w = exp(mod_score(qi, kh + j * D, D, scale, slope, i, j) - lse[row0 + i]);
+          const double g_w = w * (dot(gi_row, vh + j * D, D) - dsum[gi * (long)Sq + i]);
+          for (long d = 0; d < D; ++d) {
+            dkj[d] += scale * g_w * qi[d];
+            dvj[d] += w * gi_row[d];
+          }
+        }
+      }
+    }
+  }
+  free(dsum);
+  return 0;
+}

@@ -396,9 +396,154 @@ def pin_bwd_closed_forms(lib):
     _close(dv[0, 0], expect, 1e-13, "scale 0 causal dV")
 
 
+# ------------------------------------------------------------- score modification
+
+
+def _mask(Sq, Sk, wl, wr):
+    """Dense visibility matrix of the sliding window, built by comparison."""
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    m = np.ones((Sq, Sk), dtype=bool)
+    if wl >= 0:
+        m &= j >= i - wl
+    if wr >= 0:
+        m &= j <= i + wr
+    return m
+
+
+def pin_mod_window_zero(lib):
+    """A window of zero on both sides: query i sees key i alone, so O_i = v_i and
+    LSE_i = scale * q_i . k_i (the bias is zero at j = i)."""
+    rng = _rng(21)
+    q = _rand(rng, 1, 2, 7, 4)
+    k = _rand(rng, 1, 2, 7, 4)
+    v = _rand(rng, 1, 2, 7, 4)
+    o, lse = oracle.fwd_mod(q, k, v, 0.7, 0, 0, slopes=[0.3, -1.1], lib=lib)
+    _close(o, v, 1e-14, "window 0: O = V")
+    _close(lse, 0.7 * np.einsum("bhsd,bhsd->bhs", q, k), 1e-13, "window 0: LSE")
+
+
+def pin_mod_alibi_identical_keys(lib):
+    """All keys equal: the score is c + a*(j - i), so over the visible keys
+    lo..hi-1 the weights are a geometric sequence: LSE_i = c - a*i +
+    log(e^(a*lo) (e^(a*n) - 1) / (e^a - 1)) and O_i = sum_j w_j v_j."""
+    rng = _rng(22)
+    D, Sq, Sk = 4, 9, 11
+    q = _rand(rng, 1, 1, Sq, D)
+    kk = _rand(rng, D)
+    k = np.broadcast_to(kk, (1, 1, Sk, D)).copy()
+    v = _rand(rng, 1, 1, Sk, D)
+    a, scale, wl, wr = 0.45, 0.8, 3, 2
+    o, lse = oracle.fwd_mod(q, k, v, scale, wl, wr, slopes=[a], lib=lib)
+    for i in range(Sq):
+        lo, hi = max(0, i - wl), min(Sk, i + wr + 1)
+        n = hi - lo
+        c = scale * float(q[0, 0, i] @ kk)
+        geo = math.exp(a * lo) * math.expm1(a * n) / math.expm1(a)
+        assert abs(lse[0, 0, i] - (c - a * i + math.log(geo))) < 1e-12, f"alibi LSE row {i}"
+        w = np.exp(a * np.arange(lo, hi)) / geo
+        _close(o[0, 0, i], w @ v[0, 0, lo:hi], 1e-13, f"alibi O row {i}")
+
+
+def pin_mod_dense_brute_force(lib):
+    """A dense score matrix with the bias added and invisible pairs set to -inf,
+    reduced with scipy's logsumexp: LSE and O on random inputs, GQA."""
+    rng = _rng(23)
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 10, 13, 5
+    q = _rand(rng, B, Hq, Sq, D)
+    k = _rand(rng, B, Hkv, Sk, D)
+    v = _rand(rng, B, Hkv, Sk, D)
+    slopes = np.array([0.2, -0.5, 1.3, 0.0])
+    for wl, wr in ((4, 1), (-1, 2), (3, -1), (12, 0)):
+        o, lse = oracle.fwd_mod(q, k, v, 0.9, wl, wr, slopes=slopes, lib=lib)
+        vis = _mask(Sq, Sk, wl, wr)
+        rel = np.arange(Sk)[None, :] - np.arange(Sq)[:, None]
+        for h in range(Hq):
+            hk = h * Hkv // Hq
+            sc = 0.9 * q[0, h] @ k[0, hk].T + slopes[h] * rel
+            sc = np.where(vis, sc, -np.inf)
+            ref_lse = scipy.special.logsumexp(sc, axis=1)
+            _close(lse[0, h], ref_lse, 1e-12, f"dense LSE wl={wl} wr={wr} h={h}")
+            _close(o[0, h], np.exp(sc - ref_lse[:, None]) @ v[0, hk], 1e-12,
+                   f"dense O wl={wl} wr={wr} h={h}")
+
+
+def pin_mod_reduces_to_plain(lib):
+    """No window and no bias is the plain definition; window (-1, 0) is the causal
+    one; the row-selected form matches the full one."""
+    rng = _rng(24)
+    q = _rand(rng, 2, 2, 9, 6)
+    k = _rand(rng, 2, 1, 9, 6)
+    v = _rand(rng, 2, 1, 9, 6)
+    for wr, causal in ((-1, False), (0, True)):
+        o, lse = oracle.fwd_mod(q, k, v, 0.5, -1, wr, lib=lib)
+        o2, lse2 = oracle.fwd(q, k, v, causal, 0.5, lib=lib)
+        _close(o, o2, 1e-14, f"mod O vs plain (causal={causal})")
+        _close(lse, lse2, 1e-14, f"mod LSE vs plain (causal={causal})")
+    rows = [0, 5, 17, 35]
+    o, lse = oracle.fwd_mod(q, k, v, 0.5, 2, 3, slopes=[0.7, -0.2], lib=lib)
+    orow, lrow = oracle.fwd_rows_mod(q, k, v, 0.5, rows, 2, 3, slopes=[0.7, -0.2], lib=lib)
+    _close(orow, o.reshape(-1, 6)[rows], 1e-15, "mod rows vs full O")
+    _close(lrow, lse.reshape(-1)[rows], 1e-15, "mod rows vs full LSE")
+
+
+def _loss_mod(q, k, v, do, scale, wl, wr, slopes, lib):
+    o, _ = oracle.fwd_mod(q, k, v, scale, wl, wr, slopes=slopes, lib=lib)
+    return float(np.sum(do * o))
+
+
+def pin_mod_bwd_finite_differences(lib):
+    """Central differences (h = 1e-6, fp64) of L = sum(dO * O) under a window and
+    a bias, against the modified backward."""
+    rng = _rng(25)
+    h = 1e-6
+    for (Hq, Hkv, Sq, Sk, D, wl, wr, slopes) in [(2, 1, 7, 8, 4, 2, 1, [0.6, -0.4]),
+                                                 (1, 1, 6, 6, 4, -1, 0, [0.9])]:
+        q = _rand(rng, 1, Hq, Sq, D)
+        k = _rand(rng, 1, Hkv, Sk, D)
+        v = _rand(rng, 1, Hkv, Sk, D)
+        do = _rand(rng, 1, Hq, Sq, D)
+        dq, dk, dv, _, _ = oracle.bwd_mod(q, k, v, do, 0.6, wl, wr, slopes=slopes, lib=lib)
+        for key, g in (("q", dq), ("k", dk), ("v", dv)):
+            x = {"q": q, "k": k, "v": v}[key]
+            num = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                args = []
+                for sgn in (1, -1):
+                    xs = x.copy()
+                    xs[idx] += sgn * h
+                    a = {"q": q, "k": k, "v": v}
+                    a[key] = xs
+                    args.append(_loss_mod(a["q"], a["k"], a["v"], do, 0.6, wl, wr, slopes, lib))
+                num[idx] = (args[0] - args[1]) / (2 * h)
+            err = np.max(np.abs(num - g))
+            ref = max(np.max(np.abs(num)), 1e-3)
+            assert err <= 1e-6 * ref + 1e-9, f"mod d{key} finite differences: {err:.3e}"
+
+
+def pin_mod_bwd_invariants(lib):
+    """Rows of P still sum to one under a window and a bias: sum_j dK_j = 0 and
+    sum_j dV_j = sum_i dO_i over the group."""
+    rng = _rng(26)
+    B, Hq, Hkv, S, D = 1, 2, 1, 21, 6
+    q = _rand(rng, B, Hq, S, D, std=1.5)
+    k = _rand(rng, B, Hkv, S, D, std=1.5)
+    v = _rand(rng, B, Hkv, S, D)
+    do = _rand(rng, B, Hq, S, D)
+    dq, dk, dv, _, _ = oracle.bwd_mod(q, k, v, do, 0.5, 5, 3, slopes=[0.8, -0.3], lib=lib)
+    _close(dk.sum(axis=2), np.zeros((B, Hkv, D)), 1e-12, "mod sum_j dK_j = 0")
+    _close(dv.sum(axis=2), do.sum(axis=(1, 2)).reshape(B, Hkv, D), 1e-12,
+           "mod sum_j dV_j = sum_i dO_i")
+
+
+MOD_PINS = [pin_mod_window_zero, pin_mod_alibi_identical_keys, pin_mod_dense_brute_force,
+            pin_mod_reduces_to_plain, pin_mod_bwd_finite_differences, pin_mod_bwd_invariants]
+
 FWD_PINS = [pin_hand_example, pin_identical_keys, pin_causal_row0, pin_scale_zero,
             pin_single_key, pin_library_routines, pin_softmax_rows_sum_to_one, pin_key_permutation,
             pin_gqa_equals_repeated_mha, pin_rows_match_full, pin_pages_harness,
             pin_conditional_rescale, pin_threshold_extremes]
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_closed_forms]
-ALL_PINS = FWD_PINS + BWD_PINS
+ALL_PINS = FWD_PINS + BWD_PINS + MOD_PINS

@@ -41,6 +41,21 @@ MUTANTS = {
                   "const double dp = dot(doi, k_head + j * D, D);"),
     "dkdv_ignores_causal": ("attn_oracle.c", "for (long i = causal ? j : 0; i < Sq; ++i) {",
                             "for (long i = 0; i < Sq; ++i) {"),
+    "mod_window_left_off_by_one": ("attn_oracle.c", "if (wl >= 0 && i - wl > a) a = i - wl;",
+                                   "if (wl >= 0 && i - wl > a) a = i - wl + 1;"),
+    "mod_window_right_off_by_one": ("attn_oracle.c",
+                                    "if (wr >= 0 && i + wr + 1 < b) b = i + wr + 1;",
+                                    "if (wr >= 0 && i + wr + 1 < b) b = i + wr;"),
+    "mod_bias_sign": ("attn_oracle.c",
+                      "return scale * dot(qi, kj, D) + slope * (double)(j - i);",
+                      "return scale * dot(qi, kj, D) + slope * (double)(i - j);"),
+    "mod_slope_head_index": ("attn_oracle.c", "return slopes ? slopes[h] : 0.0;",
+                             "return slopes ? slopes[0] : 0.0;"),
+    "mod_dkdv_ignores_window": ("attn_oracle.c", "if (j < lo || j >= hi) continue;",
+                                "if (j >= hi) continue;"),
+    "mod_dq_row_term_sign": ("attn_oracle.c",
+                             "const double g_w = w * (dot(gi_row, vh + j * D, D) - rterm);",
+                             "const double g_w = w * (dot(gi_row, vh + j * D, D) + rterm);"),
     "tiled_threshold_reversed": ("tiled_body.h",
                                  "} else if (tile_max - m[r] > (REAL)threshold) {",
                                  "} else if (m[r] - tile_max > (REAL)threshold) {"),
