@@ -25,7 +25,14 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 #: every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
            "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
-           "fa_bwd_noalloc")
+           "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod")
+
+
+class ScoreMod(ctypes.Structure):
+    """fa_score_mod: a sliding window (negative sides unbounded) and optional
+    per-head relative-position bias slopes (a device pointer or None)."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("alibi_slopes", ctypes.c_void_p)]
 
 _LIB = None
 
@@ -61,7 +68,29 @@ def _bind(lib):
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i,
                                    vp]
     lib.fa_bwd_noalloc.restype = i
+    smp = ctypes.POINTER(ScoreMod)
+    lib.fa_fwd_mod.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, smp, f, vp]
+    lib.fa_fwd_mod.restype = i
+    lib.fa_bwd_mod.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, smp, f, vp,
+                               sz, i, vp]
+    lib.fa_bwd_mod.restype = i
     return lib
+
+
+def _score_mod(causal, window, alibi_slopes, Hq):
+    """The fa_score_mod for a call, or None when the plain entry point applies."""
+    if window is None and alibi_slopes is None:
+        return None
+    wl, wr = (-1, 0 if causal else -1) if window is None else window
+    if causal and window is not None:
+        raise ValueError("give the causal mask as window=(-1, 0), not with causal=True")
+    ptr = None
+    if alibi_slopes is not None:
+        if (not alibi_slopes.is_cuda or alibi_slopes.dtype != torch.float32
+                or alibi_slopes.numel() != Hq or not alibi_slopes.is_contiguous()):
+            raise TypeError("alibi_slopes must be a contiguous fp32 CUDA tensor of Hq slopes")
+        ptr = alibi_slopes.data_ptr()
+    return ScoreMod(int(wl), int(wr), ptr)
 
 
 def lib():
@@ -102,9 +131,11 @@ def _ptr(t):
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: float | None = None, out: torch.Tensor | None = None,
-        lse: torch.Tensor | None = None, stream=None):
+        lse: torch.Tensor | None = None, stream=None, window=None, alibi_slopes=None):
     """Forward attention. q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA.
 
+    ``window=(left, right)`` and ``alibi_slopes`` (fp32 [Hq]) select the score
+    modification of fa_fwd_mod (include/fa.h).
     Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] fp32, natural log).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -117,10 +148,15 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
-    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
-                      int(bool(causal)), float(scale), _stream(stream))
+    mod = _score_mod(causal, window, alibi_slopes, Hq)
+    if mod is None:
+        rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                          int(bool(causal)), float(scale), _stream(stream))
+    else:
+        rc = lib().fa_fwd_mod(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                              Sk, D, ctypes.byref(mod), float(scale), _stream(stream))
     if rc != FA_OK:
-        raise FAError("fa_fwd", rc)
+        raise FAError("fa_fwd_mod" if mod is not None else "fa_fwd", rc)
     return out, lse
 
 
@@ -130,8 +166,9 @@ def bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, deterministic=False) -> int:
 
 def bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
         deterministic: bool = False, workspace: torch.Tensor | None = None,
-        dq=None, dk=None, dv=None, stream=None):
-    """Backward attention. Returns (dq, dk, dv) bf16, same shapes as q, k, v."""
+        dq=None, dk=None, dv=None, stream=None, window=None, alibi_slopes=None):
+    """Backward attention. Returns (dq, dk, dv) bf16, same shapes as q, k, v.
+    ``window`` / ``alibi_slopes`` as in fwd (must match the forward call)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _check(t, n)
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
@@ -146,12 +183,19 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                      _ptr(dv), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
-                      _ptr(workspace), workspace.numel(), int(bool(deterministic)),
-                      _stream(stream))
+    mod = _score_mod(causal, window, alibi_slopes, Hq)
+    if mod is None:
+        rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+                          float(scale), _ptr(workspace), workspace.numel(),
+                          int(bool(deterministic)), _stream(stream))
+    else:
+        rc = lib().fa_bwd_mod(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, ctypes.byref(mod),
+                              float(scale), _ptr(workspace), workspace.numel(),
+                              int(bool(deterministic)), _stream(stream))
     if rc != FA_OK:
-        raise FAError("fa_bwd", rc)
+        raise FAError("fa_bwd_mod" if mod is not None else "fa_bwd", rc)
     return dq, dk, dv
 
 

@@ -57,6 +57,30 @@ int check_shape(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
   return FA_OK;
 }
 
+// A call's visibility window and relative-position bias (fa_score_mod).
+struct ModArgs {
+  int wl, wr;
+  const float* alibi;
+};
+
+ModArgs plain_mod(int causal) { return ModArgs{-1, causal ? 0 : -1, nullptr}; }
+
+ModArgs read_mod(const fa_score_mod* m) {
+  if (!m) return plain_mod(0);
+  return ModArgs{m->window_left < 0 ? -1 : m->window_left,
+                 m->window_right < 0 ? -1 : m->window_right, m->alibi_slopes};
+}
+
+// Every query row must see a key: the last row sees keys from Sq - 1 - wl on.
+int check_mod(const ModArgs& m, int Sq, int Sk) {
+  if (m.wl >= 0 && (long long)m.wl < (long long)Sq - Sk) return FA_ERR_INVALID_ARG;
+  if (m.alibi && (reinterpret_cast<uintptr_t>(m.alibi) & 3)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+// The exact causal window keeps the causal schedules (longest units first).
+int is_causal(const ModArgs& m) { return (m.wl < 0 && m.wr == 0) ? 1 : 0; }
+
 int check_device() {
   int dev;
   DeviceInfo info;
@@ -160,11 +184,17 @@ int fa_set_timing_events(void* start_event, void* stop_event) {
   return FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-           int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, const ModArgs& m, float scale, fa_stream_t stream) {
   t_launches = 0;
   int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc) return rc;
+  if ((rc = check_mod(m, Sq, Sk))) return rc;
   if (Sq == 0) return FA_OK;  // nothing to read or write; q, o, lse may be null
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -182,12 +212,31 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.Hkv = Hkv;
   a.Sq = Sq;
   a.Sk = Sk;
-  a.causal = causal ? 1 : 0;
+  a.causal = is_causal(m);
+  a.wl = m.wl;
+  a.wr = m.wr;
+  a.alibi = m.alibi;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_qtiles = (Sq + kTile - 1) / kTile;
   a.n_pairs = (a.n_qtiles + 1) / 2;
   a.n_units = B * Hq * a.n_pairs;
   return launch_fwd(tq, tk, tv, a, D, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, plain_mod(causal), scale, stream);
+}
+
+int fa_fwd_mod(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int Sq, int Sk, int D, const fa_score_mod* mod, float scale,
+               fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, read_mod(mod), scale, stream);
 }
 
 int fa_fwd_status(fa_stream_t stream) { return fwd_status_take(static_cast<cudaStream_t>(stream)); }
@@ -200,13 +249,19 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int
   return L.total;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
-           int Sk, int D, int causal, float scale, void* workspace, size_t workspace_bytes,
-           int deterministic, fa_stream_t stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, const ModArgs& m, float scale, void* workspace,
+             size_t workspace_bytes, int deterministic, fa_stream_t stream) {
   t_launches = 0;
   int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc) return rc;
+  if ((rc = check_mod(m, Sq, Sk))) return rc;
   // With Sq == 0 the query-side tensors are empty and may be null; dk and dv
   // are still written (as zeros).
   const bool has_q = Sq > 0;
@@ -259,14 +314,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.Sq_pad = a.n_qtiles * kTile;
   a.n_ktiles = (Sk + kTile - 1) / kTile;
   a.n_units = B * Hkv * a.n_ktiles;
+  a.causal = is_causal(m);
+  a.wl = m.wl;
+  a.wr = m.wr;
+  a.alibi = has_q ? m.alibi : nullptr;
   // longest-first snake when the streamed queries and output gradients
   // (q, dO) fit comfortably in L2
-  a.snake = (causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
-  a.causal = causal ? 1 : 0;
+  a.snake = (a.causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
   a.deterministic = deterministic ? 1 : 0;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+           int deterministic, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, plain_mod(causal),
+                  scale, workspace, workspace_bytes, deterministic, stream);
+}
+
+int fa_bwd_mod(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+               int Sk, int D, const fa_score_mod* mod, float scale, void* workspace,
+               size_t workspace_bytes, int deterministic, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, read_mod(mod), scale,
+                  workspace, workspace_bytes, deterministic, stream);
 }
 
 int fa_bwd_status(const void* workspace, fa_stream_t stream) {

@@ -64,6 +64,8 @@
 // block twice; lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -197,10 +199,36 @@ struct BwdSmem {
                             kColDK = 256 + D;
 };
 
-// first 64-row query block that kv tile j contributes to
-__device__ __forceinline__ int bwd_qblk_lo(const BwdArgs& a, int j) {
-  if (!a.causal) return 0;
-  return (j * kTile < a.Sq) ? (j * kTile) / kQB : a.n_qblk;
+// The window (wl, wr) a kernel instantiation applies: kMod reads it from the
+// arguments, the plain kernel has none or the causal one.
+template <bool kMod>
+__device__ __forceinline__ int win_left(const BwdArgs& a) {
+  return kMod ? a.wl : -1;
+}
+template <bool kMod>
+__device__ __forceinline__ int win_right(const BwdArgs& a) {
+  return kMod ? a.wr : (a.causal ? 0 : -1);
+}
+
+// 64-row query blocks [lo, hi) with a query that sees a key of kv tile j: the
+// queries from (first key - wr) to (last key + wl)
+template <bool kMod>
+__device__ __forceinline__ void bwd_qblk_range(const BwdArgs& a, int j, int& lo, int& hi) {
+  const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
+  const int k0 = j * kTile, k1 = min(a.Sk, k0 + kTile) - 1;
+  const int q_lo = wr >= 0 ? max(0, k0 - wr) : 0;
+  const int q_hi = wl >= 0 ? min(a.Sq - 1, k1 + wl) : a.Sq - 1;
+  lo = q_lo / kQB;
+  hi = q_hi >= q_lo ? q_hi / kQB + 1 : lo;
+}
+
+// First kv tile whose keys a query of block iq sees (the smallest tile whose
+// last key reaches the block's first query minus wl); the tiles that add into
+// block iq are those from it on, as bwd_qblk_range lists them.
+template <bool kMod>
+__device__ __forceinline__ int bwd_ktile_first(const BwdArgs& a, int iq) {
+  const int wl = win_left<kMod>(a);
+  return wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
 }
 
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -297,6 +325,7 @@ __device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
   return k < a.n_units ? k : -1;
 }
 
+template <bool kMod>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) {
   BwdUnit w;
   if (a.snake) {
@@ -309,13 +338,16 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
   }
   w.b = w.bhk / a.Hkv;
   w.hk = w.bhk - w.b * a.Hkv;
-  w.lo = bwd_qblk_lo(a, w.j);
-  w.n_blk = a.n_qblk - w.lo;
+  int hi;
+  bwd_qblk_range<kMod>(a, w.j, w.lo, hi);
+  w.n_blk = hi - w.lo;
   w.n_it = group * w.n_blk;
   return w;
 }
 
-template <int D>
+// kMod: a sliding window and / or the relative-position bias (a.alibi); the
+// plain kernel applies no mask or the causal one.
+template <int D, bool kMod>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -391,7 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         return true;
       };
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit(a, u, group);
+        const BwdUnit w = bwd_unit<kMod>(a, u, group);
         // The unit's first block's Q / dO go out before its K / V: its stage
         // frees up while the previous unit still holds K and V, so it has landed
         // by the time K and V can be replaced.  Later blocks follow K and V, which
@@ -443,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit(a, u, group);
+        const BwdUnit w = bwd_unit<kMod>(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (role < 2) {
@@ -572,7 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
-      const BwdUnit w = bwd_unit(a, u, group);
+      const BwdUnit w = bwd_unit<kMod>(a, u, group);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= a.Sk;
       for (int t = 0; t < w.n_it; ++t, ++it) {
@@ -599,16 +631,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_after();
         const uint32_t s_col = L::kColS + (it & 1) * kQB + c0;  // this warp's S^T columns
-        // queries c with iq*64 + c < kv are masked (causal)
-        const int causal_lim = a.causal ? kv - iq * kQB - c0 : -1;
+        // column c is query q0 + c; it sees key kv iff c_lo <= c <= c_hi
+        const int q0 = iq * kQB + c0;
+        const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
+        const int c_lo = wr >= 0 ? kv - wr - q0 : INT_MIN;
+        const int c_hi = wl >= 0 ? kv + wl - q0 : INT_MAX;
+        // -LSE2 plus the relative-position bias slope*log2(e)*(kv - q) per column
+        // (zero bias: exactly -LSE2)
+        if (kMod) {
+          const float slope2 =
+              a.alibi ? a.alibi[w.hk * group + gi] * 1.4426950408889634f : 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) lse[c] = slope2 * (float)(kv - q0 - c) - lse[c];
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) lse[c] = -lse[c];
+        }
         float p[32];
         {
           uint32_t v[32];
           tmem_ld32(t_row + s_col, v);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, -lse[c]));
-            p[c] = (row_dead || c < causal_lim) ? 0.f : x;
+            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, lse[c]));
+            p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x;
           }
         }
         {
@@ -665,7 +711,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t it = 0, unit = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-      const BwdUnit w = bwd_unit(a, u, group);
+      const BwdUnit w = bwd_unit<kMod>(a, u, group);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
@@ -685,11 +731,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int good = 1;
         if (a.deterministic && wq < kAddWarps) {
           // kv tiles add into block iq in ascending order: the semaphore counts
-          // finished adding warps, so tile j starts once it reaches j * kAddWarps
+          // finished adding warps, so tile j starts once every tile from the
+          // block's first contributor on has added (j - j_first) * kAddWarps
           int* sem = a.sem + (size_t)bh * a.n_qblk + iq;
           if (lane == 0) {
             const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(sem) < w.j * kAddWarps) {
+            const int j_first = bwd_ktile_first<kMod>(a, iq);
+            while (ld_acquire(sem) < (w.j - j_first) * kAddWarps) {
               if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
                 *abort_flag = 1;
                 good = 0;
@@ -817,7 +865,9 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (!current_device(&dev, &info)) return FA_ERR_CUDA;
   static bool attr_done[64] = {};
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(bwd_main<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bwd_main<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAllocBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_main<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAllocBytes) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_done[dev] = true;
@@ -837,6 +887,9 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   //    in-order semaphore chain relies on)
   {
     const int grid = a.n_units < sms ? a.n_units : sms;
+    // a window other than none / causal, or a bias, selects the general kernel
+    const bool mod = a.alibi || !(a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal)));
+    const auto kernel = mod ? bwd_main<D, true> : bwd_main<D, false>;
     record_timing(false, stream);
     if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
@@ -849,10 +902,10 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       attr[0].val.cooperative = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, bwd_main<D>, tq, tk, tv, tdo, a) != cudaSuccess)
+      if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
-      bwd_main<D><<<grid, kBwdThreads, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
+      kernel<<<grid, kBwdThreads, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
     }
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     record_timing(true, stream);

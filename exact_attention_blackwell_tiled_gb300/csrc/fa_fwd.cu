@@ -110,12 +110,17 @@ __device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, in
   pair = a.causal ? ((r & 1) ? (r >> 1) : (np - 1 - (r >> 1))) : r;
 }
 
-// kv tiles query tile qt needs (0 when the tile lies past Sq)
-__device__ __forceinline__ int tile_kv_count(const FwdArgs& a, int qt) {
-  if (qt * kTile >= a.Sq) return 0;
-  int kv_len = a.Sk;
-  if (a.causal) kv_len = min(a.Sk, min(a.Sq, (qt + 1) * kTile));
-  return (kv_len + kTile - 1) / kTile;
+// kv tiles [lo, hi) that query tile qt sees under the window (wl, wr) (empty
+// when the tile lies past Sq)
+__device__ __forceinline__ void tile_kv_range(const FwdArgs& a, int wl, int wr, int qt, int& lo,
+                                              int& hi) {
+  lo = hi = 0;
+  if (qt * kTile >= a.Sq) return;
+  const int last = min(a.Sq, (qt + 1) * kTile) - 1;  // last query row of the tile
+  const int lo_key = wl >= 0 ? max(0, qt * kTile - wl) : 0;
+  const int hi_key = wr >= 0 ? min(a.Sk, last + wr + 1) : a.Sk;
+  lo = lo_key / kTile;
+  hi = max(lo, (hi_key + kTile - 1) / kTile);
 }
 
 // Bounded wait done by every lane of a warp; the outcome is made warp-uniform so
@@ -133,7 +138,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D>
+// kMod: 0 plain (no mask or the causal one), 1 a sliding window, 2 a window
+// and the relative-position bias (a.alibi) added to every score.
+template <int D, int kMod>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -181,6 +188,10 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
+  constexpr bool kWin = kMod >= 1, kBias = kMod == 2;
+  // the window; plain calls carry only the causal flag
+  const int wl = kWin ? a.wl : -1;
+  const int wr = kWin ? a.wr : (a.causal ? 0 : -1);
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -204,8 +215,12 @@ __global__ void __launch_bounds__(320, 1)
         unit_coords(a, u, bh, pair);
         const int b = bh / a.Hq, h = bh - b * a.Hq;
         const int bhk = b * a.Hkv + h / group;
-        const int n0 = tile_kv_count(a, 2 * pair), n1 = tile_kv_count(a, 2 * pair + 1);
-        const int nmax = n0 > n1 ? n0 : n1;
+        int lo0, hi0, lo1, hi1;
+        tile_kv_range(a, wl, wr, 2 * pair, lo0, hi0);
+        tile_kv_range(a, wl, wr, 2 * pair + 1, lo1, hi1);
+        // the pair's kv tiles [jlo, jlo + nmax): the second tile's rows come later
+        const int jlo = lo0;
+        const int nmax = (hi1 > hi0 ? hi1 : hi0) - jlo;
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQEmpty + qs), ((q_it / L::kQStages) & 1) ^ 1, abort_flag)) {
           ok = false;
@@ -220,7 +235,7 @@ __global__ void __launch_bounds__(320, 1)
             tma_load_3d(qdst + t * L::kTileBytes + cb * L::kBlockBytes, &tm_q,
                         bar(L::kBarQFull + qs), cb * 64, (2 * pair + t) * kTile, bh);
         ++q_it;
-        for (int j = 0; j < nmax; ++j) {
+        for (int j = jlo; j < jlo + nmax; ++j) {
           if (!load_kv(&tm_k, bhk, j) || !load_kv(&tm_v, bhk, j)) { ok = false; break; }
         }
       }
@@ -243,8 +258,17 @@ __global__ void __launch_bounds__(320, 1)
       for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
         int bh, pair;
         unit_coords(a, u, bh, pair);
-        const int n[2] = {tile_kv_count(a, 2 * pair), tile_kv_count(a, 2 * pair + 1)};
-        const int nmax = n[0] > n[1] ? n[0] : n[1];
+        // kv tile j sits at position p = j - jlo of the pair's range; tile t
+        // computes S for positions [plo[t], phi[t]) and O one position behind
+        int plo[2], phi[2];
+        tile_kv_range(a, wl, wr, 2 * pair, plo[0], phi[0]);
+        tile_kv_range(a, wl, wr, 2 * pair + 1, plo[1], phi[1]);
+        const int jlo = plo[0];
+        const int nmax = (phi[1] > phi[0] ? phi[1] : phi[0]) - jlo;
+        for (int t = 0; t < 2; ++t) {
+          plo[t] -= jlo;
+          phi[t] -= jlo;
+        }
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQFull + qs), (q_it / L::kQStages) & 1, abort_flag)) {
           ok = false;
@@ -273,14 +297,14 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t k_base = sbase + L::kOffKV + k_st * L::kTileBytes;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (j >= 1 && j <= n[t]) {
+            if (j >= plo[t] + 1 && j <= phi[t]) {
               // GEMM 2: O_t += P_t(j-1) V_{j-1}
               if (!mbar_wait(bar(L::kBarPFull + t), p_seen[t] & 1, abort_flag)) {
                 ok = false;
                 break;
               }
               ++p_seen[t];
-              if (j == 1 && units_t[t] > 0 &&
+              if (j == plo[t] + 1 && units_t[t] > 0 &&
                   !mbar_wait(bar(L::kBarOFree + t), (units_t[t] - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
@@ -291,10 +315,10 @@ __global__ void __launch_bounds__(320, 1)
               for (int kk = 0; kk < kTile / 16; ++kk)
                 umma_ts_w(tmem + L::kColO + t * D, tmem + t * kTile + kk * 8,
                           v_lo + ((kk * 16 * 128) >> 4), kHi, kIdescO,
-                          (j > 1 || kk > 0) ? 1u : 0u);
-              if (j == n[t]) umma_commit(bar(L::kBarOFinal + t));
+                          (j > plo[t] + 1 || kk > 0) ? 1u : 0u);
+              if (j == phi[t]) umma_commit(bar(L::kBarOFinal + t));
             }
-            if (j < n[t]) {
+            if (j >= plo[t] && j < phi[t]) {
               // GEMM 1: S_t = Q_t K_j^T
               const uint32_t q_lo = sdesc_lo(q_base + t * L::kTileBytes, 16);
               const uint32_t k_lo = sdesc_lo(k_base, 16);
@@ -320,7 +344,7 @@ __global__ void __launch_bounds__(320, 1)
         kv_it = base_it + 2 * nmax;
         ++q_it;
         for (int t = 0; t < 2; ++t)
-          if (n[t] >= 1) ++units_t[t];
+          if (phi[t] > plo[t]) ++units_t[t];
       }
       // Every issued MMA must complete before TMEM is released.
       umma_commit(bar(L::kBarDrain));
@@ -338,17 +362,24 @@ __global__ void __launch_bounds__(320, 1)
       int bh, pair;
       unit_coords(a, u, bh, pair);
       const int qt = 2 * pair + t;
-      const int n_kv = tile_kv_count(a, qt);
-      if (n_kv == 0) continue;
+      int jlo, jhi;
+      tile_kv_range(a, wl, wr, qt, jlo, jhi);
+      if (jhi == jlo) continue;
       const int q_row = qt * kTile + r;
-      const int lim = a.causal ? min(a.Sk, q_row + 1) : a.Sk;  // keys [0, lim) visible
+      // keys [lo_row, lim) are visible to this row
+      const int lim = wr >= 0 ? min(a.Sk, q_row + wr + 1) : a.Sk;
+      const int lo_row = wl >= 0 ? max(0, q_row - wl) : 0;
+      auto hidden = [&](int key) { return key >= lim || (kWin && key < lo_row); };
+      // relative-position bias in log2 units: slope * log2(e) per key offset
+      const float slope2 = kBias ? a.alibi[bh % a.Hq] * 1.4426950408889634f : 0.f;
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = jlo; j < jhi; ++j) {
         if (!warp_wait(bar(L::kBarSFull + t), g & 1, abort_flag)) { ok = false; break; }
         ++g;
         tc_fence_after();
         const int kv0 = j * kTile;
-        const bool masked_tile = kv0 + kTile > lim;
+        const bool masked_tile = kv0 + kTile > lim || (kWin && kv0 < lo_row);
+        const float bias0 = slope2 * (float)(kv0 - q_row);  // bias of the tile's first key
         const float c = a.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
@@ -356,7 +387,7 @@ __global__ void __launch_bounds__(320, 1)
         // Conditional rescale: keep a stale running max unless the new max
         // exceeds it by more than 8 (P then stays <= 2^8).
         auto update_max = [&](float tmax) {
-          if (j == 0) {
+          if (j == jlo) {
             m_run = tmax;
           } else if (tmax > m_run + 8.0f) {
             alpha = ex2_mufu(m_run - tmax);
@@ -374,12 +405,20 @@ __global__ void __launch_bounds__(320, 1)
             if (masked_tile) {
 #pragma unroll
               for (int i = 0; i < kTile; ++i)
-                if (kv0 + i >= lim) v[i] = __float_as_uint(-INFINITY);
+                if (hidden(kv0 + i)) v[i] = __float_as_uint(-INFINITY);
             }
+            if (kBias) {
+              // the bias varies along the row: the max of s*c + bias itself
 #pragma unroll
-            for (int i = 0; i < kTile; i += 2) mraw = fmax3(mraw, u2f(v[i]), u2f(v[i + 1]));
+              for (int i = 0; i < kTile; i += 2)
+                mraw = fmax3(mraw, fmaf(u2f(v[i]), c, fmaf(slope2, (float)i, bias0)),
+                             fmaf(u2f(v[i + 1]), c, fmaf(slope2, (float)(i + 1), bias0)));
+            } else {
+#pragma unroll
+              for (int i = 0; i < kTile; i += 2) mraw = fmax3(mraw, u2f(v[i]), u2f(v[i + 1]));
+            }
           }
-          update_max(mraw == -INFINITY ? -INFINITY : mraw * c);
+          update_max(mraw == -INFINITY || kBias ? mraw : mraw * c);
           const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
           // Pass 2, one half-row (64 scores) per round trip: P = 2^(s*c - m)
           // with one packed FMA per two scores; masked columns are -inf and
@@ -395,15 +434,20 @@ __global__ void __launch_bounds__(320, 1)
             if (masked_tile) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                if (kv0 + h * 64 + i >= lim) w0[i] = __float_as_uint(-INFINITY);
-                if (kv0 + h * 64 + 32 + i >= lim) w1[i] = __float_as_uint(-INFINITY);
+                if (hidden(kv0 + h * 64 + i)) w0[i] = __float_as_uint(-INFINITY);
+                if (hidden(kv0 + h * 64 + 32 + i)) w1[i] = __float_as_uint(-INFINITY);
               }
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const uint32_t* src = (i < 16) ? w0 : w1;
               const int e = (i & 15) * 2;
-              const float2 tt = __ffma2_rn(make_float2(u2f(src[e]), u2f(src[e + 1])), c2, nm2);
+              float2 add = nm2;
+              if (kBias)  // bias of keys kv0 + h*64 + 2i, +1, minus the max
+                add = __ffma2_rn(make_float2((float)(h * 64 + 2 * i), (float)(h * 64 + 2 * i + 1)),
+                                 make_float2(slope2, slope2),
+                                 make_float2(bias0 + neg_m, bias0 + neg_m));
+              const float2 tt = __ffma2_rn(make_float2(u2f(src[e]), u2f(src[e + 1])), c2, add);
               float p0, p1;
               if ((i & 7) < L::kPolyPairs) {
                 const float2 pp = ex2_poly2(tt);
@@ -429,16 +473,18 @@ __global__ void __launch_bounds__(320, 1)
             tmem_ld32(t_row + col_s + cb * 32, w);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const bool dead = kv0 + cb * 32 + i >= lim;
+              const bool dead = hidden(kv0 + cb * 32 + i);
               const float x = u2f(w[i]);
-              if (c == 0.f)
+              if (kBias)  // s*c + bias (0 * s is 0 for the finite scores)
+                mraw = dead ? mraw : fmaxf(mraw, fmaf(x, c, fmaf(slope2, (float)(cb * 32 + i), bias0)));
+              else if (c == 0.f)
                 mraw = dead ? mraw : fmaxf(mraw, 0.f * x);
               else
                 mraw = dead ? mraw : fminf(mraw, x);
             }
           }
-          const bool none = (c == 0.f) ? (mraw == -INFINITY) : (mraw == INFINITY);
-          update_max(none ? -INFINITY : (c == 0.f ? 0.f : mraw * c));
+          const bool none = (kBias || c == 0.f) ? (mraw == -INFINITY) : (mraw == INFINITY);
+          update_max(none ? -INFINITY : (kBias ? mraw : (c == 0.f ? 0.f : mraw * c)));
           const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
@@ -450,10 +496,12 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < 32; ++i) {
               const uint32_t* src = (i < 16) ? w0 : w1;
               const int e = (i & 15) * 2, col = kv0 + h * 64 + 2 * i;
-              float p0 = ex2_mufu(fmaf(u2f(src[e]), c, neg_m));
-              float p1 = ex2_mufu(fmaf(u2f(src[e + 1]), c, neg_m));
-              if (col >= lim) p0 = 0.f;
-              if (col + 1 >= lim) p1 = 0.f;
+              const float b0 = fmaf(slope2, (float)(col - kv0), bias0) + neg_m;
+              const float b1 = fmaf(slope2, (float)(col + 1 - kv0), bias0) + neg_m;
+              float p0 = ex2_mufu(fmaf(u2f(src[e]), c, b0));
+              float p1 = ex2_mufu(fmaf(u2f(src[e + 1]), c, b1));
+              if (hidden(col)) p0 = 0.f;
+              if (hidden(col + 1)) p1 = 0.f;
               sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
             }
@@ -526,7 +574,11 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (!current_device(&dev, &info)) return FA_ERR_CUDA;
   static bool attr_done[64] = {};
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fwd_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAllocBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAllocBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAllocBytes) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_done[dev] = true;
@@ -557,7 +609,14 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     grid = a.n_units < sms ? a.n_units : sms;
   }
   record_timing(false, stream);
-  fwd_kernel<D><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  // a window other than none / causal, or a bias, selects the general kernel
+  const bool plain_window = a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal));
+  if (a.alibi)
+    fwd_kernel<D, 2><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  else if (!plain_window)
+    fwd_kernel<D, 1><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  else
+    fwd_kernel<D, 0><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   record_timing(true, stream);
   note_launches(1);

@@ -35,6 +35,10 @@ struct FwdArgs {
   int* status;
   int B, Hq, Hkv, Sq, Sk;
   int causal;
+  // visibility: key j is seen by query i iff (wl < 0 || j >= i - wl) and
+  // (wr < 0 || j <= i + wr); causal is wl = -1, wr = 0
+  int wl, wr;
+  const float* alibi;  // [Hq] slopes of the relative-position bias, or null
   float scale_log2;  // scale * log2(e)
   int n_qtiles;
   int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
@@ -64,6 +68,9 @@ struct BwdArgs {
   int B, Hq, Hkv, Sq, Sk, D;
   int Sq_pad;
   int causal;
+  // visibility window and relative-position bias, as in FwdArgs
+  int wl, wr;
+  const float* alibi;
   int deterministic;
   float scale;
   float scale_log2;

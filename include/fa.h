@@ -71,6 +71,35 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream);
 
 /*
+ * Score modification: a sliding-window mask and a linear relative-position bias
+ * (FlashAttention-4 pages, "CuTe-DSL Implementation and Rapid JIT Compilation":
+ * the FlexAttention integration's score modifications, relative position biases
+ * and masks, which the pages name without defining).  Key kv_idx is visible to
+ * query q_idx iff
+ *   (window_left  < 0 || kv_idx >= q_idx - window_left) &&
+ *   (window_right < 0 || kv_idx <= q_idx + window_right),
+ * so {-1, 0} is fa_fwd's causal mask and {-1, -1} no mask.  Every query row
+ * must see a key: window_left < 0 or window_left >= Sq - Sk (else
+ * FA_ERR_INVALID_ARG).  alibi_slopes is null or a device array of Hq fp32
+ * slopes (4-byte aligned, else FA_ERR_MISALIGNED, left unread when Sq == 0);
+ * the score of (q_idx, kv_idx) in query head h becomes
+ * scale * q.k + alibi_slopes[h] * (kv_idx - q_idx).
+ */
+typedef struct {
+  int window_left;
+  int window_right;
+  const float* alibi_slopes;
+} fa_score_mod;
+
+/*
+ * fa_fwd with a score modification; mod == NULL is fa_fwd without the causal
+ * mask.  Same tensors, sizes, pointer rules and errors as fa_fwd.
+ */
+int fa_fwd_mod(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int Sq, int Sk, int D, const fa_score_mod* mod, float scale,
+               fa_stream_t stream);
+
+/*
  * Synchronises `stream`, returns FA_OK or FA_ERR_TIMEOUT if any forward launch on
  * this device since the previous call recorded a timed-out wait, and clears the
  * record.  FA_ERR_CUDA if the synchronisation itself fails.
@@ -103,6 +132,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
            int Sk, int D, int causal, float scale, void* workspace, size_t workspace_bytes,
            int deterministic, fa_stream_t stream);
+
+/*
+ * fa_bwd with a score modification (see fa_score_mod); o and lse must come from
+ * fa_fwd_mod with the same modification.  mod == NULL is fa_bwd without the
+ * causal mask.  Same tensors, workspace, sizes, pointer rules and errors as
+ * fa_bwd.
+ */
+int fa_bwd_mod(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+               int Sk, int D, const fa_score_mod* mod, float scale, void* workspace,
+               size_t workspace_bytes, int deterministic, fa_stream_t stream);
 
 /*
  * Synchronises `stream` and returns the status the last fa_bwd recorded in

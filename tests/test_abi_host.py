@@ -107,6 +107,20 @@ def test_row_count_limit(L):
     assert L.fa_fwd(P16, P16, P16, P16, P16, 1 << 13, 2, 1, 1 << 17, 128, 64, 0, 1.0, None) == 1
 
 
+def test_score_mod_validation(L):
+    mod = fa.ScoreMod(64, -1, None)  # the last query row would see no key
+    assert L.fa_fwd_mod(P16, P16, P16, P16, P16, 1, 1, 1, 256, 128, 64, ctypes.byref(mod), 1.0,
+                        None) == 1
+    assert L.fa_bwd_mod(P16, P16, P16, P16, P16, P16, P16, P16, P16, 1, 1, 1, 256, 128, 64,
+                        ctypes.byref(mod), 1.0, P16, 1 << 30, 0, None) == 1
+    bad = fa.ScoreMod(-1, 0, 16 * 1024 + 2)  # slopes must be 4-byte aligned
+    assert L.fa_fwd_mod(P16, P16, P16, P16, P16, 1, 1, 1, 128, 128, 64, ctypes.byref(bad), 1.0,
+                        None) == 3
+    ok = fa.ScoreMod(128, -1, None)  # window_left = Sq - Sk is the smallest allowed
+    assert L.fa_fwd_mod(None, P16, P16, None, None, 1, 1, 1, 0, 128, 64, ctypes.byref(ok), 1.0,
+                        None) == 0
+
+
 def test_exp2_hook_validation(L):
     assert L.fa_exp2_test(None, None, 0, 0, None) == 0
     assert L.fa_exp2_test(None, None, -1, 0, None) == 1
