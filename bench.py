@@ -330,6 +330,8 @@ def run_ours(args):
              "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak}
     if args.sweep and rank == 0:
         extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
+    if args.mod_sweep and rank == 0:
+        extra["mod_sweep"] = mod_sweep(fa, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -380,6 +382,75 @@ def fwd_sweep(fa, dev, peak, iters=10):
     return out
 
 
+def visible_pairs(Sq: int, Sk: int, wl: int, wr: int) -> int:
+    """(query, key) pairs a window (wl, wr) leaves visible; negative = unbounded."""
+    import numpy as np
+    i = np.arange(Sq, dtype=np.int64)
+    lo = np.maximum(0, i - wl) if wl >= 0 else np.zeros_like(i)
+    hi = np.minimum(Sk - 1, i + wr) if wr >= 0 else np.full_like(i, Sk - 1)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+# B, H, S, D, window_left, window_right, bias
+MOD_SWEEP = [
+    (1, 16, 16384, 128, -1, 0, False),     # causal (the plain kernels)
+    (1, 16, 16384, 128, -1, 0, True),      # causal with the relative-position bias
+    (1, 16, 16384, 128, 1023, 0, False),   # causal local window of 1024 keys
+    (1, 16, 16384, 128, 4095, 0, False),   # causal local window of 4096 keys
+    (1, 16, 16384, 128, 512, 512, True),   # two-sided window of 1025 keys with the bias
+    (4, 16, 2048, 128, 255, 0, False),     # the train shape with a 256-key local window
+]
+
+
+def mod_sweep(fa, dev, peak, iters=10):
+    """Forward and backward-main TFLOP/s with a sliding window and / or the
+    relative-position bias; FLOPs counted over the visible (query, key) pairs."""
+    import torch
+    out = []
+    for B, H, S, D, wl, wr, bias in MOD_SWEEP:
+        gen = torch.Generator(device=dev).manual_seed(9)
+        q, k, v, do = (torch.randn(B, H, S, D, device=dev, generator=gen).to(torch.bfloat16)
+                       for _ in range(4))
+        slopes = (torch.tensor([0.5 ** (1 + h % 8) for h in range(H)], device=dev)
+                  if bias else None)
+        kw = dict(window=(wl, wr), alibi_slopes=slopes)
+        ws = torch.empty(fa.bwd_workspace_bytes(B, H, H, S, S, D), dtype=torch.uint8, device=dev)
+        o, lse = fa.fwd(q, k, v, **kw)
+        grads = [torch.empty_like(q) for _ in range(3)]
+
+        def run(which, e=None):
+            if e is not None:
+                fa.set_timing_events(*e)
+            if which == "fwd":
+                fa.fwd(q, k, v, out=o, lse=lse, **kw)
+            else:
+                fa.bwd(q, k, v, o, do, lse, workspace=ws, dq=grads[0], dk=grads[1], dv=grads[2],
+                       **kw)
+
+        ms = {}
+        for which in ("fwd", "bwd"):
+            for _ in range(3):
+                run(which)
+            torch.cuda.synchronize(dev)
+            t = []
+            for _ in range(iters):
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                run(which, e)
+                t.append(e)
+            torch.cuda.synchronize(dev)
+            ms[which] = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
+        assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
+        f_fwd = 4.0 * B * H * D * visible_pairs(S, S, wl, wr)
+        tf_f = f_fwd / (ms["fwd"] * 1e-3) / 1e12
+        tf_b = 2.5 * f_fwd / (ms["bwd"] * 1e-3) / 1e12
+        out.append({"B": B, "H": H, "S": S, "D": D, "window": [wl, wr], "bias": bias,
+                    "fwd_ms": round(ms["fwd"], 4), "fwd_tflops": round(tf_f, 1),
+                    "fwd_frac": round(tf_f / peak, 4), "bwd_main_ms": round(ms["bwd"], 4),
+                    "bwd_main_tflops": round(tf_b, 1), "bwd_main_frac": round(tf_b / peak, 4)})
+        del q, k, v, do, o, lse, ws, grads
+    return out
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -415,6 +486,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--sweep", action="store_true", help="also time the forward S/D sweep")
+    ap.add_argument("--mod-sweep", action="store_true",
+                    help="also time sliding-window / relative-position-bias attention")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for the baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
