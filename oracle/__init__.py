@@ -45,6 +45,10 @@ def _bind(lib):
     lib.oracle_bwd_units_mod.argtypes = [p, p, p, p, i, i, i, i, i, i, d, i, i, p, p,
                                          ctypes.c_int64, p, p, p, p, p]
     lib.oracle_bwd_units_mod.restype = i
+    lib.oracle_fwd_mod_range.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, i, i, p, p]
+    lib.oracle_fwd_mod_range.restype = i
+    lib.oracle_lse_merge.argtypes = [p, p, i, ctypes.c_long, i, p, p]
+    lib.oracle_lse_merge.restype = i
     for name in ("oracle_tiled_fwd_f64", "oracle_tiled_fwd_f32"):
         f = getattr(lib, name)
         f.argtypes = [p, p, p, i, i, i, i, i, i, i, d, i, i, i, d, p, p, p, p]
@@ -209,6 +213,42 @@ def bwd_mod(q, k, v, do, scale: float, window_left: int = -1, window_right: int 
     if rc:
         raise ValueError(f"oracle_bwd_units_mod rejected its arguments ({rc})")
     return dq, dk, dv, o, lse
+
+
+def fwd_mod_range(q, k, v, scale: float, k0: int, k1: int, window_left: int = -1,
+                  window_right: int = -1, slopes=None, lib=None):
+    """fwd_mod over the keys [k0, k1) only (window and bias at the absolute key
+    index).  Rows with no visible key there get O = 0, LSE = -inf."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
+    sl = _slopes(slopes, Hq)
+    o = np.zeros((B, Hq, Sq, D))
+    lse = np.zeros((B, Hq, Sq))
+    rc = lib.oracle_fwd_mod_range(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
+                                  int(window_left), int(window_right),
+                                  None if sl is None else _ptr(sl), int(k0), int(k1), _ptr(o),
+                                  _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_fwd_mod_range rejected its arguments ({rc})")
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts, lib=None):
+    """Merge n attention parts over disjoint key sets: o_parts [n, ..., D],
+    lse_parts [n, ...] (natural log, -inf = empty part).  Returns (O, LSE)."""
+    lib = lib or load()
+    op = _f64(o_parts)
+    lp = _f64(lse_parts)
+    n, D = op.shape[0], op.shape[-1]
+    assert lp.shape == op.shape[:-1], "one LSE per part row"
+    rows = int(np.prod(lp.shape[1:], dtype=np.int64))
+    o = np.zeros(op.shape[1:])
+    lse = np.zeros(lp.shape[1:])
+    rc = lib.oracle_lse_merge(_ptr(op), _ptr(lp), int(n), rows, int(D), _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_lse_merge rejected its arguments ({rc})")
+    return o, lse
 
 
 def tiled_fwd(q, k, v, causal: bool, scale: float, block_q: int = 64, block_kv: int = 64,

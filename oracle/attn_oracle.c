@@ -462,3 +462,81 @@ int oracle_bwd_units_mod(const double* q, const double* k, const double* v, cons
   free(dsum);
   return 0;
 }
+
+/*
+ * Split-KV: attention over part of the keys, and the merge of such parts.
+ *
+ * The FlashAttention-4 pages name sequence parallelism (deployment section)
+ * without a mechanism; the step it rests on is the identity behind the online
+ * softmax of the three phases ("The Asymmetric Hardware Scaling Wall"): the
+ * softmax over a union of disjoint key sets K_1 .. K_n follows from each set's
+ * own normalised output O_c and log-sum-exp LSE_c,
+ *
+ *     LSE = M + ln sum_c exp(LSE_c - M),   M = max_c LSE_c
+ *     O   = sum_c exp(LSE_c - LSE) O_c
+ *
+ * An empty part has LSE_c = -inf and weight 0; a row with no non-empty part
+ * gets O = 0 and LSE = -inf.
+ */
+
+/*
+ * Forward with the score modification restricted to the keys [k0, k1) (window
+ * and bias still use the absolute key index j).  Rows with no visible key in
+ * the range get O = 0, LSE = -inf.
+ */
+int oracle_fwd_mod_range(const double* q, const double* k, const double* v, int B, int Hq,
+                         int Hkv, int Sq, int Sk, int D, double scale, int wl, int wr,
+                         const double* slopes, int k0, int k1, double* o, double* lse) {
+  int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
+  if (rc) return rc;
+  if (k0 < 0 || k1 < k0 || k1 > Sk) return -3;
+  const long total = (long)B * Hq * Sq;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (long flat = 0; flat < total; ++flat) {
+      const long i = flat % Sq, bh = flat / Sq;
+      const long b = bh / Hq, h = bh % Hq;
+      const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
+      long lo, hi;
+      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      if (lo < k0) lo = k0;
+      if (hi > k1) hi = k1;
+      mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,
+                  scale, head_slope(slopes, h), s, o + flat * D, lse + flat);
+    }
+    free(s);
+  }
+  return 0;
+}
+
+/*
+ * Merge n parts: o_parts [n, rows, D], lse_parts [n, rows] -> o [rows, D],
+ * lse [rows].
+ */
+int oracle_lse_merge(const double* o_parts, const double* lse_parts, int n, long rows, int D,
+                     double* o, double* lse) {
+  if (n < 1 || rows < 0 || D < 1) return -1;
+#pragma omp parallel for schedule(static)
+  for (long r = 0; r < rows; ++r) {
+    double M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmax(M, lse_parts[(long)c * rows + r]);
+    double* orow = o + r * D;
+    for (long d = 0; d < D; ++d) orow[d] = 0.0;
+    if (M == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int c = 0; c < n; ++c) z += exp(lse_parts[(long)c * rows + r] - M);
+    const double row_lse = M + log(z);
+    for (int c = 0; c < n; ++c) {
+      const double w = exp(lse_parts[(long)c * rows + r] - row_lse);
+      const double* oc = o_parts + ((long)c * rows + r) * D;
+      for (long d = 0; d < D; ++d) orow[d] += w * oc[d];
+    }
+    lse[r] = row_lse;
+  }
+  return 0;
+}

@@ -538,6 +538,92 @@ def pin_mod_bwd_invariants(lib):
            "mod sum_j dV_j = sum_i dO_i")
 
 
+# --------------------------------------------------------------------------- split-KV
+
+
+def pin_split_partition(lib):
+    """The softmax over a union of disjoint key sets: the parts over any
+    partition of [0, Sk), merged, give the full attention (window, bias, GQA,
+    ragged chunks, rows with no visible key in some chunks)."""
+    rng = _rng(31)
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 19, 23, 5
+    q = _rand(rng, B, Hq, Sq, D, std=1.5)
+    k = _rand(rng, B, Hkv, Sk, D, std=1.5)
+    v = _rand(rng, B, Hkv, Sk, D)
+    slopes = np.array([0.3, -0.7, 0.0, 1.1])
+    cuts = [0, 5, 6, 17, 23]
+    for wl, wr, sl in ((4, 2, slopes), (-1, 0, None), (-1, -1, None), (6, -1, slopes)):
+        o, lse = oracle.fwd_mod(q, k, v, 0.8, wl, wr, slopes=sl, lib=lib)
+        parts = [oracle.fwd_mod_range(q, k, v, 0.8, a, b, wl, wr, slopes=sl, lib=lib)
+                 for a, b in zip(cuts[:-1], cuts[1:])]
+        if wl == 4:
+            assert any(np.isneginf(p[1]).any() for p in parts), "some rows empty in a chunk"
+        om, lm = oracle.lse_merge(np.stack([p[0] for p in parts]),
+                                  np.stack([p[1] for p in parts]), lib=lib)
+        _close(om, o, 1e-12, f"merged O wl={wl} wr={wr}")
+        _close(lm, lse, 1e-12, f"merged LSE wl={wl} wr={wr}")
+
+
+def pin_split_range_special_cases(lib):
+    """The whole key range is the unrestricted forward; an empty range gives
+    O = 0 and LSE = -inf; a one-key range gives O = v_j and LSE = the score of
+    (i, j) where j is visible, and the empty result where it is not."""
+    rng = _rng(32)
+    Sq, Sk, D = 8, 9, 4
+    q = _rand(rng, 1, 1, Sq, D)
+    k = _rand(rng, 1, 1, Sk, D)
+    v = _rand(rng, 1, 1, Sk, D)
+    wl, wr, a, scale = 2, 1, 0.4, 0.9
+    o, lse = oracle.fwd_mod(q, k, v, scale, wl, wr, slopes=[a], lib=lib)
+    o2, lse2 = oracle.fwd_mod_range(q, k, v, scale, 0, Sk, wl, wr, slopes=[a], lib=lib)
+    _close(o2, o, 0.0, "range [0, Sk) O")
+    _close(lse2, lse, 0.0, "range [0, Sk) LSE")
+    o3, lse3 = oracle.fwd_mod_range(q, k, v, scale, 3, 3, wl, wr, slopes=[a], lib=lib)
+    assert np.all(o3 == 0.0) and np.all(np.isneginf(lse3)), "empty range"
+    j = 4
+    o4, lse4 = oracle.fwd_mod_range(q, k, v, scale, j, j + 1, wl, wr, slopes=[a], lib=lib)
+    for i in range(Sq):
+        if i - wl <= j <= i + wr:
+            _close(o4[0, 0, i], v[0, 0, j], 1e-15, f"one key O row {i}")
+            ref = scale * float(q[0, 0, i] @ k[0, 0, j]) + a * (j - i)
+            assert abs(lse4[0, 0, i] - ref) < 1e-13, f"one key LSE row {i}"
+        else:
+            assert np.all(o4[0, 0, i] == 0.0) and np.isneginf(lse4[0, 0, i]), f"hidden row {i}"
+
+
+def pin_merge_closed_forms(lib):
+    """Merge weights by hand: one part is the identity; two parts with equal LSE
+    average with LSE + ln 2; LSEs ln 3 apart weigh 3/4 and 1/4 (also near
+    LSE = 1000, where exp overflows without the max shift); an empty part
+    (-inf) is ignored; all parts empty give O = 0, LSE = -inf."""
+    rng = _rng(33)
+    D = 6
+    o1, o2 = _rand(rng, 3, D), _rand(rng, 3, D)
+    l1 = np.array([0.3, -2.0, 5.0])
+    om, lm = oracle.lse_merge(o1[None], l1[None], lib=lib)
+    _close(om, o1, 0.0, "one part O")
+    _close(lm, l1, 0.0, "one part LSE")
+    om, lm = oracle.lse_merge(np.stack([o1, o2]), np.stack([l1, l1]), lib=lib)
+    _close(om, 0.5 * (o1 + o2), 1e-15, "equal parts O")
+    _close(lm, l1 + math.log(2.0), 1e-15, "equal parts LSE")
+    for base in (0.0, 1000.0, -1000.0):
+        lo = np.full(3, base)
+        om, lm = oracle.lse_merge(np.stack([o1, o2]), np.stack([lo + math.log(3.0), lo]), lib=lib)
+        # LSE near 1000 carries fp64 spacing 1.1e-13 into the weights
+        _close(om, 0.75 * o1 + 0.25 * o2, 1e-12, f"3:1 parts O at {base}")
+        _close(lm, lo + math.log(4.0), 1e-12, f"3:1 parts LSE at {base}")
+    empty = np.full(3, -np.inf)
+    om, lm = oracle.lse_merge(np.stack([o1, np.zeros_like(o2), o2 * 0]),
+                              np.stack([l1, empty, empty]), lib=lib)
+    _close(om, o1, 1e-15, "empty parts ignored: O")
+    _close(lm, l1, 1e-15, "empty parts ignored: LSE")
+    om, lm = oracle.lse_merge(np.stack([o1 * 0, o2 * 0]), np.stack([empty, empty]), lib=lib)
+    assert np.all(om == 0.0) and np.all(np.isneginf(lm)), "all parts empty"
+
+
+SPLIT_PINS = [pin_split_partition, pin_split_range_special_cases, pin_merge_closed_forms]
+
+
 MOD_PINS = [pin_mod_window_zero, pin_mod_alibi_identical_keys, pin_mod_dense_brute_force,
             pin_mod_reduces_to_plain, pin_mod_bwd_finite_differences, pin_mod_bwd_invariants]
 
@@ -546,4 +632,4 @@ FWD_PINS = [pin_hand_example, pin_identical_keys, pin_causal_row0, pin_scale_zer
             pin_gqa_equals_repeated_mha, pin_rows_match_full, pin_pages_harness,
             pin_conditional_rescale, pin_threshold_extremes]
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_closed_forms]
-ALL_PINS = FWD_PINS + BWD_PINS + MOD_PINS
+ALL_PINS = FWD_PINS + BWD_PINS + MOD_PINS + SPLIT_PINS

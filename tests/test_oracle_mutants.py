@@ -56,6 +56,14 @@ MUTANTS = {
     "mod_dq_row_term_sign": ("attn_oracle.c",
                              "const double g_w = w * (dot(gi_row, vh + j * D, D) - rterm);",
                              "const double g_w = w * (dot(gi_row, vh + j * D, D) + rterm);"),
+    "merge_lse_drops_max": ("attn_oracle.c", "const double row_lse = M + log(z);",
+                            "const double row_lse = log(z);"),
+    "merge_weights_unnormalised": ("attn_oracle.c",
+                                   "const double w = exp(lse_parts[(long)c * rows + r] - row_lse);",
+                                   "const double w = exp(lse_parts[(long)c * rows + r] - M);"),
+    "range_ignores_k0": ("attn_oracle.c", "if (lo < k0) lo = k0;", "if (lo < 0) lo = k0;"),
+    "range_upper_inclusive": ("attn_oracle.c", "if (hi > k1) hi = k1;",
+                              "if (hi > k1 + 1) hi = k1 + 1;"),
     "tiled_threshold_reversed": ("tiled_body.h",
                                  "} else if (tile_max - m[r] > (REAL)threshold) {",
                                  "} else if (m[r] - tile_max > (REAL)threshold) {"),
