@@ -332,6 +332,8 @@ def run_ours(args):
         extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
     if args.mod_sweep and rank == 0:
         extra["mod_sweep"] = mod_sweep(fa, dev, peak)
+    if args.split_sweep and rank == 0:
+        extra["split_sweep"] = split_sweep(fa, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -451,6 +453,61 @@ def mod_sweep(fa, dev, peak, iters=10):
     return out
 
 
+# B, H, Sq, Sk, D, window_right (-1: none; Sk - Sq: bottom-right causal)
+SPLIT_SWEEP = [
+    (1, 16, 1024, 32768, 128, 32768 - 1024),   # chunked prefill at the end of a 32k context
+    (1, 16, 1024, 32768, 64, 32768 - 1024),
+    (2, 16, 128, 16384, 128, -1),              # 128-query block against 16k keys
+    (1, 8, 512, 131072, 128, 131072 - 512),    # 512 queries at the end of a 128k context
+    (1, 4, 4096, 65536, 128, -1),              # few heads, long context
+]
+
+
+def split_sweep(fa, dev, peak, iters=10):
+    """Forward TFLOP/s of the split-KV path (split kernel + merge, timed together)
+    against the unsplit kernel, where the unsplit units are fewer than the SMs."""
+    import torch
+    out = []
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for B, H, Sq, Sk, D, wr in SPLIT_SWEEP:
+        gen = torch.Generator(device=dev).manual_seed(10)
+        q = torch.randn(B, H, Sq, D, device=dev, generator=gen).to(torch.bfloat16)
+        k, v = (torch.randn(B, H, Sk, D, device=dev, generator=gen).to(torch.bfloat16)
+                for _ in range(2))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, Sq, device=dev)
+        n_auto = fa.fwd_split_count(B, H, Sq, Sk, sms)
+        counts = sorted({1, max(1, n_auto // 2), n_auto, 2 * n_auto})
+        ws = torch.empty(max(fa.fwd_split_workspace_bytes(B, H, Sq, Sk, D, n) for n in counts)
+                         + 1, dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        f = 4.0 * B * H * D * visible_pairs(Sq, Sk, -1, wr)
+        row = {"B": B, "H": H, "Sq": Sq, "Sk": Sk, "D": D, "window_right": wr, "n_auto": n_auto}
+        for n in counts:
+            def run():
+                fa.fwd(q, k, v, out=o, lse=lse, window=(-1, wr), n_splits=n,
+                       split_workspace=ws)
+            for _ in range(3):
+                run()
+            torch.cuda.synchronize(dev)
+            t = []
+            for _ in range(iters):
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e[0].record(stream)
+                run()
+                e[1].record(stream)
+                t.append(e)
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
+            tf = f / (ms * 1e-3) / 1e12
+            row[f"n{n}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                            "frac": round(tf / peak, 4)}
+        assert fa.fwd_status() == fa.FA_OK
+        out.append(row)
+        del q, k, v, o, lse, ws
+    return out
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -486,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--sweep", action="store_true", help="also time the forward S/D sweep")
+    ap.add_argument("--split-sweep", action="store_true",
+                    help="also time the split-KV forward against the unsplit kernel")
     ap.add_argument("--mod-sweep", action="store_true",
                     help="also time sliding-window / relative-position-bias attention")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 #: every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
            "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
-           "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod")
+           "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod", "fa_fwd_split_count",
+           "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge")
 
 
 class ScoreMod(ctypes.Structure):
@@ -74,6 +75,14 @@ def _bind(lib):
     lib.fa_bwd_mod.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, smp, f, vp,
                                sz, i, vp]
     lib.fa_bwd_mod.restype = i
+    lib.fa_fwd_split_count.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_split_count.restype = i
+    lib.fa_fwd_split_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.fa_fwd_split_workspace_bytes.restype = sz
+    lib.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, smp, f, i, vp, sz, vp]
+    lib.fa_fwd_split.restype = i
+    lib.fa_lse_merge.argtypes = [vp, vp, i, vp, vp, i64, i, vp]
+    lib.fa_lse_merge.restype = i
     return lib
 
 
@@ -131,11 +140,14 @@ def _ptr(t):
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: float | None = None, out: torch.Tensor | None = None,
-        lse: torch.Tensor | None = None, stream=None, window=None, alibi_slopes=None):
+        lse: torch.Tensor | None = None, stream=None, window=None, alibi_slopes=None,
+        n_splits: int | None = None, split_workspace: torch.Tensor | None = None):
     """Forward attention. q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA.
 
     ``window=(left, right)`` and ``alibi_slopes`` (fp32 [Hq]) select the score
-    modification of fa_fwd_mod (include/fa.h).
+    modification of fa_fwd_mod (include/fa.h).  ``n_splits`` (0: automatic)
+    runs the split-KV form fa_fwd_split; its workspace is ``split_workspace``
+    (uint8 CUDA) or allocated here.
     Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] fp32, natural log).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -149,6 +161,20 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     mod = _score_mod(causal, window, alibi_slopes, Hq)
+    if n_splits is not None:
+        if mod is None and causal:
+            mod = ScoreMod(-1, 0, None)
+        ws_bytes = fwd_split_workspace_bytes(B, Hq, Sq, Sk, D, n_splits)
+        if split_workspace is None:
+            split_workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+        rc = lib().fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                                Sk, D, None if mod is None else ctypes.byref(mod), float(scale),
+                                int(n_splits), _ptr(split_workspace),
+                                split_workspace.numel() * split_workspace.element_size(),
+                                _stream(stream))
+        if rc != FA_OK:
+            raise FAError("fa_fwd_split", rc)
+        return out, lse
     if mod is None:
         rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
                           int(bool(causal)), float(scale), _stream(stream))
@@ -157,6 +183,40 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
                               Sk, D, ctypes.byref(mod), float(scale), _stream(stream))
     if rc != FA_OK:
         raise FAError("fa_fwd_mod" if mod is not None else "fa_fwd", rc)
+    return out, lse
+
+
+def fwd_split_count(B, Hq, Sq, Sk, sm_count: int = 0) -> int:
+    """Splits fa_fwd_split uses for n_splits = 0 (sm_count 0: current device)."""
+    return int(lib().fa_fwd_split_count(B, Hq, Sq, Sk, int(sm_count)))
+
+
+def fwd_split_workspace_bytes(B, Hq, Sq, Sk, D, n_splits: int = 0) -> int:
+    return int(lib().fa_fwd_split_workspace_bytes(B, Hq, Sq, Sk, D, int(n_splits)))
+
+
+def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor | None = None,
+              lse: torch.Tensor | None = None, stream=None):
+    """Log-sum-exp merge of parts over disjoint key sets (fa_lse_merge).
+
+    o_parts [n, ..., D] fp32 and lse_parts [n, ...] fp32 (natural log, -inf for
+    an empty part), contiguous CUDA.  Returns (o [..., D] bf16, lse [...] fp32).
+    """
+    for t, n in ((o_parts, "o_parts"), (lse_parts, "lse_parts")):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous fp32 CUDA tensor")
+    if tuple(lse_parts.shape) != tuple(o_parts.shape[:-1]):
+        raise ValueError("lse_parts must be o_parts' shape without the last dimension")
+    n, D = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel() if n > 0 else 0
+    if out is None:
+        out = torch.empty(o_parts.shape[1:], dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    rc = lib().fa_lse_merge(_ptr(o_parts), _ptr(lse_parts), int(n), _ptr(out), _ptr(lse),
+                            int(rows), int(D), _stream(stream))
+    if rc != FA_OK:
+        raise FAError("fa_lse_merge", rc)
     return out, lse
 
 

@@ -189,38 +189,115 @@ int fa_set_timing_events(void* start_event, void* stop_event) {
 namespace fa {
 namespace {
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-             int Hkv, int Sq, int Sk, int D, const ModArgs& m, float scale, fa_stream_t stream) {
-  t_launches = 0;
+// Validation, tensor maps and the forward arguments shared by the plain and
+// split entry points.  *nothing = true when Sq == 0 (valid, no work).
+int fwd_setup(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+              int Hkv, int Sq, int Sk, int D, const ModArgs& m, float scale, CUtensorMap* tq,
+              CUtensorMap* tk, CUtensorMap* tv, FwdArgs* a, bool* nothing) {
+  *nothing = false;
   int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc) return rc;
   if ((rc = check_mod(m, Sq, Sk))) return rc;
-  if (Sq == 0) return FA_OK;  // nothing to read or write; q, o, lse may be null
+  if (Sq == 0) {  // nothing to read or write; q, o, lse may be null
+    *nothing = true;
+    return FA_OK;
+  }
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
   if ((rc = check_device())) return rc;
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_bsd(&tq, q, B * Hq, Sq, D) || !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) ||
-      !make_tmap_bsd(&tv, v, B * Hkv, Sk, D))
+  if (!make_tmap_bsd(tq, q, B * Hq, Sq, D) || !make_tmap_bsd(tk, k, B * Hkv, Sk, D) ||
+      !make_tmap_bsd(tv, v, B * Hkv, Sk, D))
     return FA_ERR_CUDA;
-  FwdArgs a{};
-  a.o = o;
-  a.lse = lse;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.Sq = Sq;
-  a.Sk = Sk;
-  a.causal = is_causal(m);
-  a.wl = m.wl;
-  a.wr = m.wr;
-  a.alibi = m.alibi;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.n_qtiles = (Sq + kTile - 1) / kTile;
-  a.n_pairs = (a.n_qtiles + 1) / 2;
-  a.n_units = B * Hq * a.n_pairs;
+  *a = FwdArgs{};
+  a->o = o;
+  a->lse = lse;
+  a->B = B;
+  a->Hq = Hq;
+  a->Hkv = Hkv;
+  a->Sq = Sq;
+  a->Sk = Sk;
+  a->causal = is_causal(m);
+  a->wl = m.wl;
+  a->wr = m.wr;
+  a->alibi = m.alibi;
+  a->scale_log2 = scale * 1.4426950408889634f;
+  a->n_qtiles = (Sq + kTile - 1) / kTile;
+  a->n_pairs = (a->n_qtiles + 1) / 2;
+  a->n_units = B * Hq * a->n_pairs;
+  a->n_split = 1;
+  a->split_tiles = 0;
+  return FA_OK;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, const ModArgs& m, float scale, fa_stream_t stream) {
+  t_launches = 0;
+  CUtensorMap tq, tk, tv;
+  FwdArgs a;
+  bool nothing;
+  const int rc = fwd_setup(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, m, scale, &tq, &tk, &tv, &a,
+                           &nothing);
+  if (rc || nothing) return rc;
   return launch_fwd(tq, tk, tv, a, D, static_cast<cudaStream_t>(stream));
+}
+
+constexpr int kMaxAutoSplits = 64;
+constexpr int kSplitUnitOverhead = 3;  // fixed cost of a unit, in kv tiles (Q load, epilogue)
+
+// Split plan: the effective split count for a request and the kv tiles per
+// split.  A request of 0 picks, when the units are fewer than the SMs, the
+// count that minimises (waves of units) x (kv tiles per split + the fixed
+// cost of a unit), ties to the smaller count.  0 on invalid sizes.
+int split_plan(int B, int Hq, int Sq, int Sk, int n_req, int sms, int* tiles_per_split) {
+  if (B < 1 || Hq < 1 || Sq < 0 || Sk < 1 || n_req < 0) return 0;
+  const long long n_kv = ((long long)Sk + kTile - 1) / kTile;
+  const long long pairs = (((long long)Sq + kTile - 1) / kTile + 1) / 2;
+  const long long units = (long long)B * Hq * (pairs > 0 ? pairs : 1);
+  auto effective = [&](long long n, long long* per) {
+    if (n > n_kv) n = n_kv;
+    if (n < 1) n = 1;
+    *per = (n_kv + n - 1) / n;
+    return (n_kv + *per - 1) / *per;  // no empty split
+  };
+  long long per = 0, n = 0;
+  if (n_req > 0) {
+    n = effective(n_req, &per);
+  } else {
+    if (sms < 1) return 0;
+    n = effective(1, &per);
+    if (units < sms) {
+      long long best = -1;
+      for (long long c = 1; c <= kMaxAutoSplits && c <= n_kv; ++c) {
+        long long pc;
+        const long long nc = effective(c, &pc);
+        const long long waves = (nc * units + sms - 1) / sms;
+        const long long cost = waves * (pc + kSplitUnitOverhead);
+        if (best < 0 || cost < best) {
+          best = cost;
+          n = nc;
+          per = pc;
+        }
+      }
+    }
+  }
+  if (tiles_per_split) *tiles_per_split = (int)per;
+  return (int)n;
+}
+
+int current_sm_count() {
+  int dev;
+  DeviceInfo info;
+  if (!current_device(&dev, &info)) return 0;
+  return info.sm_count;
+}
+
+// fp32 parts of O [n, rows, D], then (256-byte aligned) of LSE [n, rows].
+size_t split_o_bytes(int n, long long rows, int D) {
+  return ((size_t)n * (size_t)rows * D * sizeof(float) + 255) & ~(size_t)255;
+}
+size_t split_ws_bytes(int n, long long rows, int D) {
+  return split_o_bytes(n, rows, D) + (size_t)n * (size_t)rows * sizeof(float);
 }
 
 }  // namespace
@@ -240,6 +317,66 @@ int fa_fwd_mod(const void* q, const void* k, const void* v, void* o, float* lse,
 }
 
 int fa_fwd_status(fa_stream_t stream) { return fwd_status_take(static_cast<cudaStream_t>(stream)); }
+
+int fa_fwd_split_count(int B, int Hq, int Sq, int Sk, int sm_count) {
+  const int sms = sm_count > 0 ? sm_count : current_sm_count();
+  return split_plan(B, Hq, Sq, Sk, 0, sms, nullptr);
+}
+
+size_t fa_fwd_split_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int n_splits) {
+  if (D != 64 && D != 128) return 0;
+  const int n = split_plan(B, Hq, Sq, Sk, n_splits, n_splits == 0 ? current_sm_count() : 1,
+                           nullptr);
+  if (n <= 1) return 0;
+  return split_ws_bytes(n, (long long)B * Hq * Sq, D);
+}
+
+int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int D, const fa_score_mod* mod, float scale,
+                 int n_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  t_launches = 0;
+  if (n_splits < 0) return FA_ERR_INVALID_ARG;
+  const ModArgs m = read_mod(mod);
+  CUtensorMap tq, tk, tv;
+  FwdArgs a;
+  bool nothing;
+  int rc = fwd_setup(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, m, scale, &tq, &tk, &tv, &a,
+                     &nothing);
+  if (rc || nothing) return rc;
+  int per = 0;
+  const int n = split_plan(B, Hq, Sq, Sk, n_splits, n_splits == 0 ? current_sm_count() : 1, &per);
+  if (n < 1) return FA_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n == 1) return launch_fwd(tq, tk, tv, a, D, st);
+  const long long rows = (long long)B * Hq * Sq;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < split_ws_bytes(n, rows, D))
+    return FA_ERR_WORKSPACE;
+  if ((long long)B * Hq * a.n_pairs * n > INT32_MAX) return FA_ERR_INVALID_ARG;
+  a.n_split = n;
+  a.split_tiles = per;
+  a.n_units = B * Hq * a.n_pairs * n;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + split_o_bytes(n, rows, D));
+  if ((rc = launch_fwd(tq, tk, tv, a, D, st))) return rc;
+  MergeArgs mg{a.o_part, a.lse_part, n, rows, o, lse};
+  return launch_merge(mg, D, st);
+}
+
+int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+                 int64_t rows, int D, fa_stream_t stream) {
+  t_launches = 0;
+  if (n_parts < 1 || rows < 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (rows == 0) return FA_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse_parts) & 3) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3))
+    return FA_ERR_MISALIGNED;
+  int rc;
+  if ((rc = check_device())) return rc;
+  MergeArgs mg{o_parts, lse_parts, n_parts, (long long)rows, o, lse};
+  return launch_merge(mg, D, static_cast<cudaStream_t>(stream));
+}
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
   (void)deterministic;

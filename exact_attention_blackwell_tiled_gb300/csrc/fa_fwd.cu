@@ -97,8 +97,19 @@ __device__ __forceinline__ int cta_unit(const FwdArgs& a, int r) {
 //                inside a head so contiguous chunks carry near-equal work.
 //   sched 2:     longest pairs of every head first (causal work grows with the
 //                pair index), used when all K/V fit in L2.
-__device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& pair) {
+//   sched 3:     split-KV; the pairs of one (head, split) are adjacent, so
+//                they run together and share that split's K/V in L2.
+__device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& pair,
+                                            int& split) {
   const int np = a.n_pairs;
+  split = 0;
+  if (a.sched == 3) {
+    const int rest = u / np;
+    pair = u - rest * np;
+    bh = rest / a.n_split;
+    split = rest - bh * a.n_split;
+    return;
+  }
   if (a.sched == 2) {
     const int BH = a.B * a.Hq;
     pair = np - 1 - u / BH;
@@ -123,6 +134,39 @@ __device__ __forceinline__ void tile_kv_range(const FwdArgs& a, int wl, int wr, 
   hi = max(lo, (hi_key + kTile - 1) / kTile);
 }
 
+// A tile's range cut to the kv tiles of `split` (kSplit); may become empty.
+template <bool kSplit>
+__device__ __forceinline__ void split_kv_range(const FwdArgs& a, int wl, int wr, int qt, int split,
+                                               int& lo, int& hi) {
+  tile_kv_range(a, wl, wr, qt, lo, hi);
+  if (kSplit) {
+    const int s0 = split * a.split_tiles;
+    lo = max(lo, s0);
+    hi = max(lo, min(hi, s0 + a.split_tiles));
+  }
+}
+
+// The kv tiles the two query tiles of a pair stream: lo[t], hi[t] per tile,
+// and their union [jlo, jlo + nmax).  An empty tile gets lo = hi = jlo; both
+// empty: nmax = 0 and the unit is skipped.
+template <bool kSplit>
+__device__ __forceinline__ void pair_kv_span(const FwdArgs& a, int wl, int wr, int pair, int split,
+                                             int lo[2], int hi[2], int& jlo, int& nmax) {
+  split_kv_range<kSplit>(a, wl, wr, 2 * pair, split, lo[0], hi[0]);
+  split_kv_range<kSplit>(a, wl, wr, 2 * pair + 1, split, lo[1], hi[1]);
+  const bool e0 = hi[0] <= lo[0], e1 = hi[1] <= lo[1];
+  if (e0 && e1) {
+    jlo = lo[0];
+    nmax = 0;
+    return;
+  }
+  jlo = e0 ? lo[1] : (e1 ? lo[0] : min(lo[0], lo[1]));
+  const int jend = e0 ? hi[1] : (e1 ? hi[0] : max(hi[0], hi[1]));
+  nmax = jend - jlo;
+  if (e0) lo[0] = hi[0] = jlo;
+  if (e1) lo[1] = hi[1] = jlo;
+}
+
 // Bounded wait done by every lane of a warp; the outcome is made warp-uniform so
 // the warp-collective tcgen05.ld/st that follow are never reached by part of it.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -139,8 +183,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // kMod: 0 plain (no mask or the causal one), 1 a sliding window, 2 a window
-// and the relative-position bias (a.alibi) added to every score.
-template <int D, int kMod>
+// and the relative-position bias (a.alibi) added to every score.  kSplit: a
+// unit covers one split of the kv tiles and writes fp32 parts for the merge.
+template <int D, int kMod, bool kSplit>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -211,16 +256,13 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
       for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
-        int bh, pair;
-        unit_coords(a, u, bh, pair);
+        int bh, pair, split;
+        unit_coords(a, u, bh, pair, split);
         const int b = bh / a.Hq, h = bh - b * a.Hq;
         const int bhk = b * a.Hkv + h / group;
-        int lo0, hi0, lo1, hi1;
-        tile_kv_range(a, wl, wr, 2 * pair, lo0, hi0);
-        tile_kv_range(a, wl, wr, 2 * pair + 1, lo1, hi1);
-        // the pair's kv tiles [jlo, jlo + nmax): the second tile's rows come later
-        const int jlo = lo0;
-        const int nmax = (hi1 > hi0 ? hi1 : hi0) - jlo;
+        int lo[2], hi[2], jlo, nmax;
+        pair_kv_span<kSplit>(a, wl, wr, pair, split, lo, hi, jlo, nmax);
+        if (nmax == 0) continue;
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQEmpty + qs), ((q_it / L::kQStages) & 1) ^ 1, abort_flag)) {
           ok = false;
@@ -256,15 +298,13 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t units_t[2] = {0u, 0u};  // units with work, per tile (O-free phases)
       bool ok = true;
       for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
-        int bh, pair;
-        unit_coords(a, u, bh, pair);
+        int bh, pair, split;
+        unit_coords(a, u, bh, pair, split);
         // kv tile j sits at position p = j - jlo of the pair's range; tile t
         // computes S for positions [plo[t], phi[t]) and O one position behind
-        int plo[2], phi[2];
-        tile_kv_range(a, wl, wr, 2 * pair, plo[0], phi[0]);
-        tile_kv_range(a, wl, wr, 2 * pair + 1, plo[1], phi[1]);
-        const int jlo = plo[0];
-        const int nmax = (phi[1] > phi[0] ? phi[1] : phi[0]) - jlo;
+        int plo[2], phi[2], jlo, nmax;
+        pair_kv_span<kSplit>(a, wl, wr, pair, split, plo, phi, jlo, nmax);
+        if (nmax == 0) continue;
         for (int t = 0; t < 2; ++t) {
           plo[t] -= jlo;
           phi[t] -= jlo;
@@ -359,13 +399,18 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t g = 0, nu = 0;  // S-full phases and units consumed by this group
     bool ok = true;
     for (int ri = 0, u = cta_unit(a, 0); ok && u >= 0; u = cta_unit(a, ++ri)) {
-      int bh, pair;
-      unit_coords(a, u, bh, pair);
+      int bh, pair, split;
+      unit_coords(a, u, bh, pair, split);
       const int qt = 2 * pair + t;
       int jlo, jhi;
-      tile_kv_range(a, wl, wr, qt, jlo, jhi);
-      if (jhi == jlo) continue;
+      split_kv_range<kSplit>(a, wl, wr, qt, split, jlo, jhi);
       const int q_row = qt * kTile + r;
+      const size_t part_row = ((size_t)split * a.B * a.Hq + bh) * a.Sq + q_row;
+      if (jhi == jlo) {
+        // no key of this split reaches the tile: an empty part
+        if (kSplit && q_row < a.Sq) a.lse_part[part_row] = -INFINITY;
+        continue;
+      }
       // keys [lo_row, lim) are visible to this row
       const int lim = wr >= 0 ? min(a.Sk, q_row + wr + 1) : a.Sk;
       const int lo_row = wl >= 0 ? max(0, q_row - wl) : 0;
@@ -530,8 +575,34 @@ __global__ void __launch_bounds__(320, 1)
       if (!warp_wait(bar(L::kBarOFinal + t), nu & 1, abort_flag)) { ok = false; break; }
       ++nu;
       tc_fence_after();
-      const float inv_l = 1.0f / l_run;
       const bool row_ok = q_row < a.Sq;
+      if (kSplit) {
+        // fp32 part: O / l and the part's LSE; a row with no visible key in
+        // this split (l = 0) is an empty part, O = 0 and LSE = -inf
+        const bool empty = !(l_run > 0.f);
+        const float inv = empty ? 0.f : 1.0f / l_run;
+        float* prow = a.o_part + (row_ok ? part_row : 0) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(t_row + col_o + c * 32, v);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(u2f(v[4 * i]) * inv, u2f(v[4 * i + 1]) * inv,
+                                   u2f(v[4 * i + 2]) * inv, u2f(v[4 * i + 3]) * inv);
+          }
+        }
+        if (row_ok)
+          a.lse_part[part_row] =
+              empty ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarOFree + t));
+        continue;
+      }
+      const float inv_l = 1.0f / l_run;
       __nv_bfloat16* orow =
           reinterpret_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.Sq + (row_ok ? q_row : 0)) * D;
 #pragma unroll 1
@@ -574,13 +645,14 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (!current_device(&dev, &info)) return FA_ERR_CUDA;
   static bool attr_done[64] = {};
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(fwd_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAllocBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(fwd_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAllocBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(fwd_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAllocBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
+    const void* kernels[] = {
+        (const void*)fwd_kernel<D, 0, false>, (const void*)fwd_kernel<D, 1, false>,
+        (const void*)fwd_kernel<D, 2, false>, (const void*)fwd_kernel<D, 0, true>,
+        (const void*)fwd_kernel<D, 1, true>,  (const void*)fwd_kernel<D, 2, true>};
+    for (const void* k : kernels)
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAllocBytes) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
     attr_done[dev] = true;
   }
   int* status = nullptr;
@@ -590,7 +662,11 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const int sms = info.sm_count;
   int grid;
   const double kv_bytes = 2.0 * a.B * a.Hkv * (double)a.Sk * D * 2;
-  if (a.causal && kv_bytes <= 64.0 * (1 << 20)) {
+  if (a.n_split > 1) {
+    a.sched = 3;
+    a.chunk = 0;
+    grid = a.n_units < sms ? a.n_units : sms;
+  } else if (a.causal && kv_bytes <= 64.0 * (1 << 20)) {
     // all K/V fit comfortably in L2: longest-first snake over every head
     a.sched = 2;
     a.chunk = 0;
@@ -611,12 +687,17 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   record_timing(false, stream);
   // a window other than none / causal, or a bias, selects the general kernel
   const bool plain_window = a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal));
-  if (a.alibi)
-    fwd_kernel<D, 2><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-  else if (!plain_window)
-    fwd_kernel<D, 1><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-  else
-    fwd_kernel<D, 0><<<grid, 320, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  const int mode = a.alibi ? 2 : (plain_window ? 0 : 1);
+  const dim3 blk(320);
+  if (a.n_split > 1) {
+    if (mode == 2) fwd_kernel<D, 2, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+    else if (mode == 1) fwd_kernel<D, 1, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+    else fwd_kernel<D, 0, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  } else {
+    if (mode == 2) fwd_kernel<D, 2, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+    else if (mode == 1) fwd_kernel<D, 1, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+    else fwd_kernel<D, 0, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   record_timing(true, stream);
   note_launches(1);

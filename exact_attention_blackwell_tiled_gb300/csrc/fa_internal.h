@@ -44,12 +44,30 @@ struct FwdArgs {
   int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
   int n_units;
   int sched;  // 0: round robin over head-major units; 1: contiguous chunks of
-              // `chunk` units; 2: longest-first snake over all heads
+              // `chunk` units; 2: longest-first snake over all heads; 3: split-KV,
+              // units (head, split, pair) round robin
   int chunk;
+  // split-KV: split s holds kv tiles [s * split_tiles, (s + 1) * split_tiles);
+  // each (query tile, split) writes its own normalised O and LSE to the parts
+  int n_split;
+  int split_tiles;
+  float* o_part;    // [n_split, B * Hq, Sq, D]
+  float* lse_part;  // [n_split, B * Hq, Sq], natural log, -inf: no visible key
 };
 
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdArgs& a, int D, cudaStream_t stream);
+
+// Log-sum-exp merge of n attention parts over disjoint key sets.
+struct MergeArgs {
+  const float* o_part;    // [n, rows, D] fp32, normalised per part
+  const float* lse_part;  // [n, rows], natural log, -inf = empty part
+  int n;
+  long long rows;
+  void* o;     // [rows, D] bf16
+  float* lse;  // [rows]
+};
+int launch_merge(const MergeArgs& m, int D, cudaStream_t stream);
 int fwd_status_take(cudaStream_t stream);
 int launch_exp2_test(const float* x, float* y, int64_t n, int which, cudaStream_t stream);
 

@@ -150,6 +150,68 @@ int fa_bwd_mod(const void* q, const void* k, const void* v, const void* o, const
  */
 int fa_bwd_status(const void* workspace, fa_stream_t stream);
 
+/*
+ * Split-KV forward: the kv tiles (128 keys each) are cut into n contiguous
+ * splits, every (128-row query tile, split) is an independent unit of work, and
+ * the splits' partial results are merged by log-sum-exp (fa_lse_merge below).
+ * This fills the GPU when B * Hq * ceil(Sq / 256) units are fewer than its SMs
+ * (short query blocks against a long context).  The pages name sequence
+ * parallelism ("Production Deployment Guide": distributed sequence parallelism
+ * configurations) without a mechanism; this is its single-GPU form.
+ *
+ * fa_fwd_split_count: the number of splits fa_fwd_split uses when asked for
+ * n_splits = 0.  With units = B * Hq * ceil(ceil(Sq / 128) / 2): 1 when
+ * units >= sm_count; otherwise the n in 1..64 (and at most the kv tiles
+ * ceil(Sk / 128)) that minimises ceil(n * units / sm_count) * (tiles + 3),
+ * where tiles = ceil(kv tiles / n) is the length of a split and 3 the fixed
+ * cost of a unit in kv tiles; ties go to the smaller n, and n is reduced so
+ * that no split is empty.  sm_count <= 0 uses the current device's count.
+ * Returns 0 on invalid sizes or when no device can be queried.
+ */
+int fa_fwd_split_count(int B, int Hq, int Sq, int Sk, int sm_count);
+
+/*
+ * Workspace bytes fa_fwd_split needs for n_splits (0: the automatic count on
+ * the current device): fp32 parts of O [n, B, Hq, Sq, D] and of LSE
+ * [n, B, Hq, Sq] for the effective split count n (a request above the kv tile
+ * count, or one that would leave a split empty, is reduced).  0 when the
+ * effective count is 1 (no workspace needed) or on invalid sizes.
+ */
+size_t fa_fwd_split_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int n_splits);
+
+/*
+ * fa_fwd_mod computed as n_splits key splits and a merge (two kernels).  Same
+ * tensors, sizes, score modification and errors as fa_fwd_mod; mod == NULL is
+ * no mask.  n_splits >= 0 (0: automatic, see fa_fwd_split_count); an effective
+ * count of 1 runs fa_fwd_mod itself and ignores the workspace.  Otherwise the
+ * workspace is a caller-owned device buffer of at least
+ * fa_fwd_split_workspace_bytes(B, Hq, Sq, Sk, D, n_splits) bytes, 16-byte
+ * aligned (else FA_ERR_WORKSPACE); it is scratch, its contents on return are
+ * unspecified.  The result matches fa_fwd_mod up to the rounding of the
+ * merge (O passes through fp32 parts, then one bf16 rounding).
+ */
+int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int D, const fa_score_mod* mod, float scale,
+                 int n_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Log-sum-exp merge of n_parts attention results over disjoint key sets of the
+ * same queries (the identity behind the online softmax, "The Asymmetric
+ * Hardware Scaling Wall" phases: rescale by the exponential of the change in
+ * the max).  Per row r:
+ *   M = max_c lse_parts[c][r],  lse[r] = M + ln sum_c exp(lse_parts[c][r] - M),
+ *   o[r] = sum_c exp(lse_parts[c][r] - lse[r]) * o_parts[c][r]
+ *   o_parts   [n_parts, rows, D] fp32, each part normalised by its own sum
+ *   lse_parts [n_parts, rows] fp32, natural log; -inf marks an empty part,
+ *             whose o_parts row is not read
+ *   o [rows, D] bf16 out, lse [rows] fp32 out
+ * A row whose parts are all empty gets o = 0 and lse = -inf.  rows >= 0
+ * (0 is a no-op), n_parts >= 1, D in {64, 128}; o_parts and o 16-byte
+ * aligned, lse_parts and lse 4-byte aligned (else FA_ERR_MISALIGNED).
+ */
+int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+                 int64_t rows, int D, fa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(int status);
 
@@ -165,7 +227,8 @@ const char* fa_status_string(int status);
  */
 int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream);
 
-/* Number of kernels the last fa_fwd / fa_bwd call on this thread launched. */
+/* Number of kernels the last forward, backward or merge call on this thread
+ * launched. */
 int fa_last_launch_count(void);
 
 /*

@@ -121,6 +121,56 @@ def test_score_mod_validation(L):
                         None) == 0
 
 
+def test_split_plan(L):
+    """The automatic split count minimises waves x (split length + 3), is capped by
+    the kv tiles, never leaves a split empty, and sizes the fp32 parts of O and
+    LSE.  Expected counts worked by hand over every candidate."""
+    # 64 units, 256 kv tiles: n = 7 -> 37 tiles, 448 units = 3 waves, cost 120;
+    # n = 3: 2 waves of 89; n = 6: 3 waves of 46; n = 14: 6 waves of 22
+    assert L.fa_fwd_split_count(1, 16, 1024, 32768, 152) == 7
+    assert L.fa_fwd_split_count(1, 16, 16384, 16384, 152) == 1  # enough units already
+    # 16 units, 128 kv tiles: n = 9 -> 15 tiles, 144 units in one wave, cost 18
+    assert L.fa_fwd_split_count(2, 8, 128, 16384, 152) == 9
+    assert L.fa_fwd_split_count(1, 1, 1, 300, 152) == 3         # only 3 kv tiles
+    assert L.fa_fwd_split_count(0, 16, 1024, 32768, 152) == 0   # invalid sizes
+    assert L.fa_fwd_split_count(1, 16, 1024, 0, 152) == 0
+    # 5 requested over 256 kv tiles: 52 per split, 5 splits; 16 * 1024 rows
+    rows = 16 * 1024
+    assert L.fa_fwd_split_workspace_bytes(1, 16, 1024, 32768, 128, 5) == 5 * rows * (128 + 1) * 4
+    # 7 requested over 3 kv tiles: 3 splits; 1600 rows at D = 64
+    assert L.fa_fwd_split_workspace_bytes(1, 16, 100, 300, 64, 7) == 3 * 1600 * (64 + 1) * 4
+    # 4 requested over 10 kv tiles: 3 per split -> 4 splits; 3 requested: 4 per split -> 3
+    assert L.fa_fwd_split_workspace_bytes(1, 1, 128, 1280, 64, 4) == 4 * 128 * 65 * 4
+    assert L.fa_fwd_split_workspace_bytes(1, 1, 128, 1280, 64, 3) == 3 * 128 * 65 * 4
+    assert L.fa_fwd_split_workspace_bytes(1, 16, 1024, 32768, 128, 1) == 0  # no split
+    assert L.fa_fwd_split_workspace_bytes(1, 16, 1024, 32768, 96, 5) == 0   # bad D
+
+
+def test_split_validation(L):
+    def split(n=3, ws=P16, wsb=1 << 30, q=P16, Sq=256, mod=None):
+        return L.fa_fwd_split(q, P16, P16, P16, P16, 1, 2, 2, Sq, 1024, 64, mod, 0.125, n, ws,
+                              wsb, None)
+    assert split(n=-1) == 1
+    assert split(q=None) == 1
+    assert split(q=P17) == 3
+    assert split(Sq=0, q=None) == 0  # nothing to do
+    bad = fa.ScoreMod(10, -1, None)  # leaves the last rows without a key
+    assert split(Sq=2048, mod=ctypes.byref(bad)) == 1
+
+
+def test_merge_validation(L):
+    def merge(op=P16, lp=P16, n=2, o=P16, lse=P16, rows=10, D=128):
+        return L.fa_lse_merge(op, lp, n, o, lse, rows, D, None)
+    assert merge(rows=0, op=None, lp=None, o=None, lse=None) == 0
+    assert merge(n=0) == 1
+    assert merge(rows=-1) == 1
+    assert merge(D=96) == 2
+    assert merge(op=None) == 1
+    assert merge(op=P17) == 3
+    assert merge(o=ctypes.c_void_p(16 * 1024 + 8)) == 3
+    assert merge(lp=ctypes.c_void_p(16 * 1024 + 2)) == 3
+
+
 def test_exp2_hook_validation(L):
     assert L.fa_exp2_test(None, None, 0, 0, None) == 0
     assert L.fa_exp2_test(None, None, -1, 0, None) == 1
