@@ -466,7 +466,7 @@ int oracle_bwd_units_mod(const double* q, const double* k, const double* v, cons
 /*
  * Split-KV: attention over part of the keys, and the merge of such parts.
  *
- * The FlashAttention-4 pages name sequence parallelism (deployment section)
+ * The FlashAttention-4 pages name sequence parallelism ("Production Deployment Guide")
  * without a mechanism; the step it rests on is the identity behind the online
  * softmax of the three phases ("The Asymmetric Hardware Scaling Wall"): the
  * softmax over a union of disjoint key sets K_1 .. K_n follows from each set's
