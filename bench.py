@@ -253,7 +253,9 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # Timed region: whole steps bracketed by events, nothing recorded between
+    # the kernels (an event there would serialise their programmatic overlap).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     launches = 0
     barrier(world, dev)
     torch.cuda.synchronize(dev)
@@ -262,13 +264,22 @@ def run_ours(args):
             flush.zero_()  # L2 flush outside the timed interval
             e = ev[i]
             e[0].record(stream)
-            launches += step(time_kernels=((e[2], e[3]), (e[4], e[5])))
+            launches += step()
             e[1].record(stream)
         torch.cuda.synchronize(dev)
     barrier(world, dev)
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    fwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    bwd_main_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    # Per-kernel breakdown (the roofline's launch duration): a separate run with
+    # events around the forward kernel and the backward main kernel.
+    n_k = min(args.steps, 200)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_k)]
+    for i in range(n_k):
+        flush.zero_()
+        e = kev[i]
+        step(time_kernels=((e[0], e[1]), (e[2], e[3])))
+    torch.cuda.synchronize(dev)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    bwd_main_ms = [e[2].elapsed_time(e[3]) for e in kev]
     total_ms_local = sum(step_ms)
     total_ms = max_over_ranks(total_ms_local, world, dev)
     ms_per_step = total_ms / args.steps
@@ -469,6 +480,7 @@ def split_sweep(fa, dev, peak, iters=10):
     import torch
     out = []
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    hbm_peak = float(load_peaks()[0]["hbm_gbs"])
     for B, H, Sq, Sk, D, wr in SPLIT_SWEEP:
         gen = torch.Generator(device=dev).manual_seed(10)
         q = torch.randn(B, H, Sq, D, device=dev, generator=gen).to(torch.bfloat16)
@@ -503,6 +515,29 @@ def split_sweep(fa, dev, peak, iters=10):
             row[f"n{n}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
                             "frac": round(tf / peak, 4)}
         assert fa.fwd_status() == fa.FA_OK
+        # the merge alone, on the automatic count's parts: HBM-bound
+        if n_auto > 1:
+            rows = B * H * Sq
+            parts_o = torch.randn(n_auto, rows, D, device=dev)
+            parts_l = torch.randn(n_auto, rows, device=dev)
+            for _ in range(3):
+                fa.lse_merge(parts_o, parts_l, out=o.view(rows, D), lse=lse.view(rows))
+            flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+            t = []
+            for _ in range(iters):
+                flush.zero_()  # the parts would otherwise sit in L2
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e[0].record(stream)
+                fa.lse_merge(parts_o, parts_l, out=o.view(rows, D), lse=lse.view(rows))
+                e[1].record(stream)
+                t.append(e)
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
+            nbytes = rows * (n_auto * (4 * D + 4) + 2 * D + 4)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            row["merge"] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1),
+                            "frac_hbm": round(gbs / hbm_peak, 4)}
+            del parts_o, parts_l, flush
         out.append(row)
         del q, k, v, o, lse, ws
     return out

@@ -95,6 +95,8 @@ constexpr int kPreUnroll = 4;
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess(const BwdArgs a) {
+  grid_dep_wait();    // O (the forward's output) must be complete
+  grid_dep_launch();  // the main kernel may launch once every block runs
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerStep = 32 / kLanesPerRow;
   constexpr int kRowsPerWarp = kRowsPerStep * kPreUnroll;
@@ -401,6 +403,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above overlaps the preprocess kernel; its outputs (LSE2,
+  // Delta, the cleared dQ accumulator and semaphores) are read from here on
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
 
@@ -834,6 +840,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
+  grid_dep_wait();  // every dQ reduction of the main kernel must be complete
   // 8 elements (two 16-byte loads, one 16-byte store) per thread; row indices
   // over all heads are 32-bit (the host bounds them)
   constexpr uint32_t kPerRow = D / 8;
@@ -880,8 +887,8 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks > 8LL * sms) blocks = 8LL * sms;
     if (blocks < 1) blocks = 1;
-    bwd_preprocess<D><<<(int)blocks, 256, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_pdl(bwd_preprocess<D>, dim3((int)blocks), dim3(256), 0, stream, a) != cudaSuccess)
+      return FA_ERR_CUDA;
   }
   // 2. main: one CTA per SM (all resident, which the deterministic mode's
   //    in-order semaphore chain relies on)
@@ -905,7 +912,9 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
-      kernel<<<grid, kBwdThreads, L::kAllocBytes, stream>>>(tq, tk, tv, tdo, a);
+      if (launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), L::kAllocBytes, stream, tq, tk, tv,
+                     tdo, a) != cudaSuccess)
+        return FA_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     record_timing(true, stream);
@@ -916,8 +925,9 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     const long long total = (long long)a.B * a.Hq * a.Sq * (D / 8);
     long long blocks = (total + 255) / 256;
     if (blocks > 16LL * sms) blocks = 16LL * sms;
-    bwd_dq_convert<D><<<(int)blocks, 256, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_pdl(bwd_dq_convert<D>, dim3((int)blocks), dim3(256), 0, stream, a) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
     ++launches;
   }
   note_launches(launches);

@@ -231,6 +231,10 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above overlaps the previous kernel in the stream; q, k, v
+  // (which it may have written) are read from here on
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
   constexpr bool kWin = kMod >= 1, kBias = kMod == 2;
@@ -415,8 +419,11 @@ __global__ void __launch_bounds__(320, 1)
       const int lim = wr >= 0 ? min(a.Sk, q_row + wr + 1) : a.Sk;
       const int lo_row = wl >= 0 ? max(0, q_row - wl) : 0;
       auto hidden = [&](int key) { return key >= lim || (kWin && key < lo_row); };
-      // relative-position bias in log2 units: slope * log2(e) per key offset
+      // relative-position bias in log2 units: slope * log2(e) per key offset,
+      // and the same per unit of raw score (slope2 / c) for the max pass
       const float slope2 = kBias ? a.alibi[bh % a.Hq] * 1.4426950408889634f : 0.f;
+      const float kslope = kBias ? slope2 / a.scale_log2 : 0.f;
+      const bool kslope_ok = kBias && a.scale_log2 > 0.f && fabsf(kslope) < 1e30f;
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = jlo; j < jhi; ++j) {
         if (!warp_wait(bar(L::kBarSFull + t), g & 1, abort_flag)) { ok = false; break; }
@@ -452,8 +459,14 @@ __global__ void __launch_bounds__(320, 1)
               for (int i = 0; i < kTile; ++i)
                 if (hidden(kv0 + i)) v[i] = __float_as_uint(-INFINITY);
             }
-            if (kBias) {
-              // the bias varies along the row: the max of s*c + bias itself
+            if (kBias && kslope_ok) {
+              // the bias varies along the row: with c > 0 the max of
+              // s*c + slope2*i + bias0 is c * max(s + k*i) + bias0, k = slope2 / c
+#pragma unroll
+              for (int i = 0; i < kTile; i += 2)
+                mraw = fmax3(mraw, fmaf(kslope, (float)i, u2f(v[i])),
+                             fmaf(kslope, (float)(i + 1), u2f(v[i + 1])));
+            } else if (kBias) {
 #pragma unroll
               for (int i = 0; i < kTile; i += 2)
                 mraw = fmax3(mraw, fmaf(u2f(v[i]), c, fmaf(slope2, (float)i, bias0)),
@@ -463,7 +476,8 @@ __global__ void __launch_bounds__(320, 1)
               for (int i = 0; i < kTile; i += 2) mraw = fmax3(mraw, u2f(v[i]), u2f(v[i + 1]));
             }
           }
-          update_max(mraw == -INFINITY || kBias ? mraw : mraw * c);
+          if (mraw != -INFINITY) mraw = kBias ? (kslope_ok ? fmaf(mraw, c, bias0) : mraw) : mraw * c;
+          update_max(mraw);
           const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
           // Pass 2, one half-row (64 scores) per round trip: P = 2^(s*c - m)
           // with one packed FMA per two scores; masked columns are -inf and
@@ -688,17 +702,14 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // a window other than none / causal, or a bias, selects the general kernel
   const bool plain_window = a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal));
   const int mode = a.alibi ? 2 : (plain_window ? 0 : 1);
-  const dim3 blk(320);
-  if (a.n_split > 1) {
-    if (mode == 2) fwd_kernel<D, 2, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-    else if (mode == 1) fwd_kernel<D, 1, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-    else fwd_kernel<D, 0, true><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-  } else {
-    if (mode == 2) fwd_kernel<D, 2, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-    else if (mode == 1) fwd_kernel<D, 1, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-    else fwd_kernel<D, 0, false><<<grid, blk, L::kAllocBytes, stream>>>(tq, tk, tv, a);
-  }
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs);
+  const KernelFn kernels[2][3] = {{fwd_kernel<D, 0, false>, fwd_kernel<D, 1, false>,
+                                   fwd_kernel<D, 2, false>},
+                                  {fwd_kernel<D, 0, true>, fwd_kernel<D, 1, true>,
+                                   fwd_kernel<D, 2, true>}};
+  if (launch_pdl(kernels[a.n_split > 1 ? 1 : 0][mode], dim3(grid), dim3(320), L::kAllocBytes,
+                 stream, tq, tk, tv, a) != cudaSuccess)
+    return FA_ERR_CUDA;
   record_timing(true, stream);
   note_launches(1);
   return FA_OK;

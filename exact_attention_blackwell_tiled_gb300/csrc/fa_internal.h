@@ -109,6 +109,25 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
 
 void note_launches(int n);
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream is still running, so it must call
+// grid_dep_wait before touching memory that kernel may write.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Events requested by fa_set_timing_events for the next main-kernel launch on
 // this thread; record_timing(true/false) records start/stop and clears after stop.
 void record_timing(bool stop, cudaStream_t stream);
