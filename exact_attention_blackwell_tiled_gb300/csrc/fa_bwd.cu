@@ -30,22 +30,23 @@
 //                      bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
 //
-// bwd_main warp roles (512 threads):
-//   warps 0-7   P^T / dS^T: warp w serves key rows 32*(w%4).. (its TMEM lanes)
-//               and query columns 32*(w/4).. of the block, so each SM
-//               sub-partition runs two of them and one's latencies hide
-//               behind the other's work;
-//   warps 8-11  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
-//   warp 12     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
-//               block into a 3-stage ring;
-//   warp 13     TMEM owner; one thread issues S^T;
-//   warp 14     one thread issues dP^T;
-//   warp 15     one thread issues dV, dK and dQ^T.
+// bwd_main warp roles, with n = 8 softmax warps (plain kernel: 512 threads,
+// 128 registers) or n = 16 (score-modified kernel: 768 threads, 80 registers):
+//   warps 0..n-1  P^T / dS^T: warp w serves key rows 32*(w%4).. (its TMEM
+//                 lanes) and query columns c*(w/4).. of the block, c = 4*64/n
+//                 (32 or 16), so each SM sub-partition runs n/4 of them and
+//                 their latencies hide behind each other's work;
+//   warps n..n+3  dQ drain (one head-dim row per thread) and the dK/dV epilogue;
+//   warp n+4      TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i
+//                 per block into a 3-stage ring;
+//   warp n+5      TMEM owner; one thread issues S^T;
+//   warp n+6      one thread issues dP^T;
+//   warp n+7      one thread issues dV, dK and dQ^T.
 // TMEM columns: S^T double buffer [0,64) [64,128); P^T and dS^T (bf16 pairs)
-// replace it in place: query columns 32h..32h+31 of S^T are read by the warps
-// of half h, which then write their 16 columns of P^T and 16 of dS^T over
-// them (P^T at 32h, dS^T at 32h+16), so the two halves never touch each
-// other's columns;
+// replace it in place: query columns cp..cp+c-1 of S^T are read by the warps
+// of part p, which then write their c/2 columns of P^T and c/2 of dS^T over
+// them (P^T at cp, dS^T at cp+c/2), so the parts never touch each other's
+// columns;
 // dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
 // Three issuing threads: a thread that has MMAs queued and then waits on a
 // barrier only continues once the tensor core has taken those MMAs, so a lone
@@ -73,17 +74,24 @@ namespace fa {
 
 constexpr int kQB = 64;  // query rows per backward block
 
-// bwd_main warp roles
-constexpr int kBwdSmxWarps = 8;     // warps 0-7: P^T / dS^T
-constexpr int kBwdDrainWarp0 = 8;   // warps 8-11: dQ drain, dK/dV epilogue
-constexpr int kBwdTmaWarp = 12;
-constexpr int kBwdScoreWarp = 13;   // TMEM owner, S^T issuer
-constexpr int kBwdDPWarp = 14;      // dP^T issuer
-constexpr int kBwdGradWarp = 15;    // dV / dK / dQ^T issuer
-static_assert(kBwdDPWarp == kBwdScoreWarp + 1 && kBwdGradWarp == kBwdScoreWarp + 2,
-              "the issuers' role is warp - kBwdScoreWarp");
-constexpr int kBwdThreads = 32 * (kBwdGradWarp + 1);
-constexpr int kBwdSmxThreads = 32 * kBwdSmxWarps;
+// bwd_main warp roles.  The score-modified kernel (masks, bias: more softmax
+// work per score) runs 16 softmax warps of 16 query columns each, 768 threads
+// at 80 registers; the plain kernel 8 of 32 columns, 512 threads at 128
+// registers, which measured faster there.
+template <bool kMod>
+struct BwdRoles {
+  static constexpr int kSmxWarps = kMod ? 16 : 8;  // warps 0..: P^T / dS^T
+  static constexpr int kSmxCols = 4 * kQB / kSmxWarps;  // query columns per softmax warp
+  static constexpr int kDrainWarp0 = kSmxWarps;    // 4 warps: dQ drain, dK/dV epilogue
+  static constexpr int kTmaWarp = kDrainWarp0 + 4;
+  static constexpr int kScoreWarp = kTmaWarp + 1;  // TMEM owner, S^T issuer
+  static constexpr int kDPWarp = kScoreWarp + 1;   // dP^T issuer
+  static constexpr int kGradWarp = kScoreWarp + 2;  // dV / dK / dQ^T issuer
+  static constexpr int kThreads = 32 * (kGradWarp + 1);
+  static constexpr int kSmxThreads = 32 * kSmxWarps;
+  static_assert(kSmxCols == 16 || kSmxCols == 32, "softmax warp column split");
+  static_assert(kDrainWarp0 % 4 == 0, "drain warp q reads TMEM lane quarter q");
+};
 
 // ------------------------------------------------------------------ preprocess
 
@@ -299,6 +307,42 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// n consecutive 32-bit columns of this thread's lane (n = 8, 16, 32), waited.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "tmem_ld width");
+  if constexpr (N == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]);
+
+// Writes n consecutive 32-bit columns of this thread's lane (no wait).
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&w)[N]) {
+  static_assert(N == 8 || N == 16, "tmem_st width");
+  if constexpr (N == 16) {
+    tmem_st16(taddr, w);
+  } else {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -350,11 +394,12 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
 // plain kernel applies no mask or the causal one.
 template <int D, bool kMod>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdRoles<kMod>::kThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
   using L = BwdSmem<D>;
+  using R = BwdRoles<kMod>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -377,8 +422,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kBarPReady + s), kBwdSmxThreads);
-      mbar_init(bar(L::kBarDSReady + s), kBwdSmxThreads);
+      mbar_init(bar(L::kBarPReady + s), R::kSmxThreads);
+      mbar_init(bar(L::kBarDSReady + s), R::kSmxThreads);
     }
     mbar_init(bar(L::kBarDPFull), 1);
     mbar_init(bar(L::kBarDQFull), 1);
@@ -390,11 +435,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == kBwdScoreWarp) {
+  if (warp == R::kScoreWarp) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kBwdTmaWarp && lane == 0) {
+  if (warp == R::kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -410,7 +455,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
 
-  if (warp == kBwdTmaWarp) {
+  if (warp == R::kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0, unit = 0;
@@ -467,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (uint32_t n = (it > (uint32_t)L::kStages ? it - L::kStages : 0); n < it; ++n)
         drain_wait_b(bar(L::kBarQFull + n % L::kStages), (n / L::kStages) & 1);
     }
-  } else if (warp >= kBwdScoreWarp) {
+  } else if (warp >= R::kScoreWarp) {
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kQB, false, false);  // S^T, dP^T
@@ -477,7 +522,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // is the second column block of K (D = 128) or, at D = 64, the first again.
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
       constexpr uint32_t kHi = sdesc_hi(1024);
-      const int role = warp - kBwdScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
+      const int role = warp - R::kScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
@@ -551,10 +596,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               break;
             }
             tc_fence_after();
-            // query columns 16kk..16kk+15 of P^T / dS^T: half kk/2 of the block
+            // query columns 16kk..16kk+15 of P^T / dS^T: softmax warp part
+            // 16kk / kSC, whose columns hold P^T in the first half and dS^T in
+            // the second (two bf16 per column)
+            constexpr int kSC = R::kSmxCols;
+            auto p_col = [&](int kk) {
+              return s_col + (16 * kk / kSC) * kSC + ((16 * kk) % kSC) / 2;
+            };
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk)  // dV += P^T dO  (K = queries)
-              umma_ts_w(tmem + L::kColDV, tmem + s_col + (kk >> 1) * 32 + (kk & 1) * 8,
+              umma_ts_w(tmem + L::kColDV, tmem + p_col(kk),
                         do_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc,
                         (t > 0 || kk > 0) ? 1u : 0u);
             if (!mbar_wait(bar(L::kBarDSReady + (it & 1)), (it >> 1) & 1, abort_flag)) {
@@ -564,7 +615,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk)  // dK += dS^T Q
-              umma_ts_w(tmem + L::kColDK, tmem + s_col + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+              umma_ts_w(tmem + L::kColDK, tmem + p_col(kk) + kSC / 2,
                         q_mn_lo + ((kk * 16 * 128) >> 4), kHi, kIdAcc,
                         (t > 0 || kk > 0) ? 1u : 0u);
             // S^T, dP^T (done before the softmax warps published P^T / dS^T),
@@ -599,12 +650,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       umma_commit(bar(L::kBarDrain + role));
       drain_wait_b(bar(L::kBarDrain + role), 0);
     }
-  } else if (warp < kBwdSmxWarps) {
+  } else if (warp < R::kSmxWarps) {
     // ------------------------------------------------------------ P^T / dS^T
+    constexpr int kSC = R::kSmxCols;
     const int quarter = warp & 3;  // TMEM lanes 32*quarter.. = key rows
-    const int half = warp >> 2;    // query columns 32*half..
+    const int part = warp >> 2;    // query columns kSC*part..
     const int r = quarter * 32 + lane;
-    const int c0 = half * 32;
+    const int c0 = part * kSC;
     const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* ds_rows = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
@@ -624,10 +676,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
-        // this warp's 32 LSE2 values, loaded while S^T is still being computed
-        float lse[32];
+        // this warp's LSE2 values, loaded while S^T is still being computed
+        float lse[kSC];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < kSC / 4; ++q) {
           const float4 x = s_lse2[q];
           lse[4 * q] = x.x, lse[4 * q + 1] = x.y, lse[4 * q + 2] = x.z, lse[4 * q + 3] = x.w;
         }
@@ -648,58 +700,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float slope2 =
               a.alibi ? a.alibi[w.hk * group + gi] * 1.4426950408889634f : 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) lse[c] = slope2 * (float)(kv - q0 - c) - lse[c];
+          for (int c = 0; c < kSC; ++c) lse[c] = slope2 * (float)(kv - q0 - c) - lse[c];
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) lse[c] = -lse[c];
+          for (int c = 0; c < kSC; ++c) lse[c] = -lse[c];
         }
-        float p[32];
+        float p[kSC];
         {
-          uint32_t v[32];
-          tmem_ld32(t_row + s_col, v);
+          uint32_t v[kSC];
+          tmem_ld<kSC>(t_row + s_col, v);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < kSC; ++c) {
             const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, lse[c]));
             p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x;
           }
         }
         {
-          uint32_t wbuf[16];
+          uint32_t wbuf[kSC / 2];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) wbuf[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-          tmem_st16(t_row + s_col, wbuf);  // P^T over the first 16 of these columns
+          for (int e = 0; e < kSC / 2; ++e) wbuf[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+          tmem_st<kSC / 2>(t_row + s_col, wbuf);  // P^T over the first half of these columns
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         mbar_arrive(bar(L::kBarPReady + (it & 1)));
-        float dl[32];
+        float dl[kSC];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < kSC / 4; ++q) {
           const float4 x = s_delta[q];
           dl[4 * q] = x.x, dl[4 * q + 1] = x.y, dl[4 * q + 2] = x.z, dl[4 * q + 3] = x.w;
         }
         if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint32_t wbuf[16];
+        uint32_t wbuf[kSC / 2];
         {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColDP + c0, v);
+          uint32_t v[kSC];
+          tmem_ld<kSC>(t_row + L::kColDP + c0, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < kSC / 2; ++e) {
             const float d0 = p[2 * e] * (u2f(v[2 * e]) - dl[2 * e]);
             const float d1 = p[2 * e + 1] * (u2f(v[2 * e + 1]) - dl[2 * e + 1]);
             wbuf[e] = pack_bf16x2(d0, d1);
           }
         }
-        // dS^T over the last 16 of this warp's S^T columns (their S values were
-        // consumed above), so the dP^T columns are free as soon as they are read
-        tmem_st16(t_row + s_col + 16, wbuf);
+        // dS^T over the second half of this warp's S^T columns (their S values
+        // were consumed above), so the dP^T columns are free as soon as read
+        tmem_st<kSC / 2>(t_row + s_col + kSC / 2, wbuf);
         // shared memory, 128-byte swizzle: [key row][64 queries]; this warp's
-        // queries are 16-byte chunks 4*half .. 4*half+3
+        // queries are the 16-byte chunks (kSC/8)*part ..
         uint8_t* ds_row = ds_rows + (it % L::kDSBufs) * L::kDSBytes;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int chunk = half * 4 + ch;
+        for (int ch = 0; ch < kSC / 8; ++ch) {
+          const int chunk = part * (kSC / 8) + ch;
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
               make_uint4(wbuf[ch * 4], wbuf[ch * 4 + 1], wbuf[ch * 4 + 2], wbuf[ch * 4 + 3]);
         }
@@ -711,8 +763,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-    const int r = threadIdx.x - 32 * kBwdDrainWarp0;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
-    const int wq = warp - kBwdDrainWarp0;
+    const int r = threadIdx.x - 32 * R::kDrainWarp0;  // TMEM lane: head-dim row of dQ^T, key row of dK/dV
+    const int wq = warp - R::kDrainWarp0;
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
@@ -728,10 +780,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // Row r of dQ^T (head-dim index r, 64 queries) goes straight from TMEM
         // to the fp32 accumulator: for each query the 32 lanes of a warp add
         // 32 consecutive floats, one 128-byte line per instruction.
-        uint32_t v[kQB];
-        tmem_ld64(t_row + L::kColDQ, v);  // one round trip
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarDQEmpty));
         float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
         constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
@@ -754,12 +802,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           good = __shfl_sync(0xffffffffu, good, 0);
           __syncwarp();
         }
-        if (good && r < D) {
+        // two 32-column halves, so that only 32 values are live at a time; the
+        // columns are released once the second half is read
 #pragma unroll
-          for (int e = 0; e < kQB; ++e)
-            asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
-                         "f"(u2f(v[e]))
-                         : "memory");
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[32];
+          tmem_ld32(t_row + L::kColDQ + hf * 32, v);
+          if (hf == 1) {
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDQEmpty));
+          }
+          if (good && r < D) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(
+                               dst + (size_t)(hf * 32 + e) * D),
+                           "f"(u2f(v[e]))
+                           : "memory");
+          }
         }
         if (a.deterministic && wq < kAddWarps && good) {
           __threadfence();
@@ -781,46 +841,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int row0 = w.j * kTile + wq * 32 + grp;  // first key row of the lane group
       __nv_bfloat16* dk_base = reinterpret_cast<__nv_bfloat16*>(a.dk) + (size_t)w.bhk * a.Sk * D;
       __nv_bfloat16* dv_base = reinterpret_cast<__nv_bfloat16*>(a.dv) + (size_t)w.bhk * a.Sk * D;
+      // 32 columns of dK, then of dV, per pass (the register budget of 768
+      // threads holds one 32-column group at a time)
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t vk[32], vv[32];
+      for (int pass = 0; pass < 2 * (D / 32); ++pass) {
+        const int c = pass >> 1;
+        const bool is_v = (pass & 1) != 0;
+        uint32_t vk[32];
         __syncwarp();
         if (w.n_it > 0) {
-          tmem_ld32(t_row + L::kColDK + c * 32, vk);
-          tmem_ld32(t_row + L::kColDV + c * 32, vv);
+          tmem_ld32(t_row + (is_v ? L::kColDV : L::kColDK) + c * 32, vk);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) vk[e] = vv[e] = 0u;
+          for (int e = 0; e < 32; ++e) vk[e] = 0u;
         }
-        if (c == D / 32 - 1) {
+        if (pass == 2 * (D / 32) - 1) {
           // every TMEM read of dK / dV is done: the accumulators are free
           tc_fence_before();
           mbar_arrive(bar(L::kBarDKVEmpty));
         }
-        uint32_t wk[16], wv[16];
+        const float sc = is_v ? 1.f : a.scale;
+        uint32_t wk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          wk[e] = pack_bf16x2(u2f(vk[2 * e]) * a.scale, u2f(vk[2 * e + 1]) * a.scale);
-          wv[e] = pack_bf16x2(u2f(vv[2 * e]), u2f(vv[2 * e + 1]));
-        }
+        for (int e = 0; e < 16; ++e) wk[e] = pack_bf16x2(u2f(vk[2 * e]) * sc, u2f(vk[2 * e + 1]) * sc);
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {  // word wd of each 16-byte piece
           uint32_t xk[4] = {wk[wd], wk[4 + wd], wk[8 + wd], wk[12 + wd]};
-          uint32_t xv[4] = {wv[wd], wv[4 + wd], wv[8 + wd], wv[12 + wd]};
           xpose4(xk, lane);
-          xpose4(xv, lane);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) wk[4 * m + wd] = xk[m], wv[4 * m + wd] = xv[m];
+          for (int m = 0; m < 4; ++m) wk[4 * m + wd] = xk[m];
         }
         // wk[4m..4m+3] is now piece pc of row row0 + m
+        __nv_bfloat16* base = is_v ? dv_base : dk_base;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           if (row0 + m < a.Sk) {
             const size_t off = (size_t)(row0 + m) * D + c * 32 + pc * 8;
-            *reinterpret_cast<uint4*>(dk_base + off) =
+            *reinterpret_cast<uint4*>(base + off) =
                 make_uint4(wk[4 * m], wk[4 * m + 1], wk[4 * m + 2], wk[4 * m + 3]);
-            *reinterpret_cast<uint4*>(dv_base + off) =
-                make_uint4(wv[4 * m], wv[4 * m + 1], wv[4 * m + 2], wv[4 * m + 3]);
           }
         }
       }
@@ -829,7 +887,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kBwdScoreWarp) {
+  if (warp == R::kScoreWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -897,11 +955,12 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     // a window other than none / causal, or a bias, selects the general kernel
     const bool mod = a.alibi || !(a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal)));
     const auto kernel = mod ? bwd_main<D, true> : bwd_main<D, false>;
+    const int threads = mod ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;
     record_timing(false, stream);
     if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(kBwdThreads);
+      cfg.blockDim = dim3(threads);
       cfg.dynamicSmemBytes = L::kAllocBytes;
       cfg.stream = stream;
       cudaLaunchAttribute attr[1];
@@ -912,7 +971,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
-      if (launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), L::kAllocBytes, stream, tq, tk, tv,
+      if (launch_pdl(kernel, dim3(grid), dim3(threads), L::kAllocBytes, stream, tq, tk, tv,
                      tdo, a) != cudaSuccess)
         return FA_ERR_CUDA;
     }
