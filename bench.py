@@ -37,6 +37,7 @@ import synth  # noqa: E402
 METRIC = "attention fwd/bwd TFLOPs/s (BF16, 1×GB300) and % of tensor-core peak"
 UNIT = "TFLOP/s"
 WORKLOAD = synth.TRAIN  # B=4, Hq=Hkv=16, S=2048, D=128, causal
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -377,7 +378,12 @@ def run_ours(args):
     extra = {"fwd_tflops": round(fwd_tf, 1), "fwd_ms": round(fwd_avg, 4),
              "bwd_main_tflops": round(bwd_tf, 1), "bwd_main_ms": round(bwd_avg, 4),
              "bwd_total_flops_tflops_incl_pre_post": None,
-             "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak}
+             "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak,
+             # the vendor's dense bf16 figure for one GB300 (2.25 PFLOP/s without
+             # sparsity), the like-for-like denominator of a "% of theoretical peak"
+             "nominal_dense_bf16_tflops": NOMINAL_DENSE_BF16_TFLOPS,
+             "fwd_frac_of_nominal": round(fwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4),
+             "bwd_main_frac_of_nominal": round(bwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4)}
     if args.sweep and rank == 0:
         extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
     if args.mod_sweep and rank == 0:
