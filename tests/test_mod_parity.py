@@ -137,3 +137,52 @@ def test_zero_bias_matches_no_bias():
     o2, l2 = fa.fwd(q, k, v, window=(40, 10), alibi_slopes=torch.zeros(2, device=DEV))
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
     assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+def test_fwd_mod_full_size_sampled():
+    """A causal 1024-key window with the bias at full size (B=1, H=16, S=16384,
+    D=128, the shape the bench's score-modification sweep times): sampled rows of
+    every head against the oracle's row routine."""
+    B, H, S, D, wl, wr = 1, 16, 16384, 128, 1023, 0
+    w = synth.Workload("mod_full", B, H, H, S, S, D, False, 30)
+    q, k, v = synth.make_inputs(w)
+    slopes = _slopes(H, True)
+    o, lse = fa.fwd(q.to(DEV), k.to(DEV), v.to(DEV), scale=w.softmax_scale, window=(wl, wr),
+                    alibi_slopes=slopes.to(DEV))
+    torch.cuda.synchronize()
+    assert fa.fwd_status() == fa.FA_OK
+    rng = np.random.default_rng(8)
+    rows = np.concatenate([h * S + np.concatenate([[0, 1023, 1024, S - 1], rng.integers(0, S, 4)])
+                           for h in range(H)])
+    o_r, lse_r = oracle.fwd_rows_mod(q, k, v, w.softmax_scale, rows, wl, wr, slopes=slopes)
+    o64 = o.float().cpu().double().numpy().reshape(-1, D)[rows]
+    l64 = lse.cpu().double().numpy().reshape(-1)[rows]
+    assert_fwd_close(o64, l64, o_r, lse_r, "mod full size sampled")
+
+
+@pytest.mark.parametrize("deterministic", [False, True], ids=["atomic", "det"])
+def test_bwd_mod_sampled_units(deterministic):
+    """A two-sided window with the bias, GQA 2, at S = 4096: two kv-head units
+    of the backward against the fp64 backward."""
+    B, Hq, Hkv, S, D, wl, wr = 1, 8, 4, 4096, 128, 700, 300
+    w = synth.Workload("mod_bwd_units", B, Hq, Hkv, S, S, D, False, 31, with_do=True)
+    q, k, v, do = synth.make_inputs(w, with_do=True)
+    slopes = _slopes(Hq, True)
+    sd = slopes.to(DEV)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, scale=w.softmax_scale, window=(wl, wr), alibi_slopes=sd)
+    ws = torch.empty(fa.bwd_workspace_bytes(B, Hq, Hkv, S, S, D, deterministic),
+                     dtype=torch.uint8, device=DEV)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, scale=w.softmax_scale,
+                        deterministic=deterministic, workspace=ws, window=(wl, wr),
+                        alibi_slopes=sd)
+    assert fa.bwd_status(ws) == fa.FA_OK
+    units = [0, Hkv - 1]
+    dq_r, dk_r, dv_r, _, _ = oracle.bwd_mod(q, k, v, do, w.softmax_scale, wl, wr, slopes=slopes,
+                                            units=units)
+    g = Hq // Hkv
+    for u in units:
+        hs = slice(u * g, (u + 1) * g)
+        assert_grad_close(dq[0, hs], dq_r[0, hs], f"dQ unit {u}")
+        assert_grad_close(dk[0, u], dk_r[0, u], f"dK unit {u}")
+        assert_grad_close(dv[0, u], dv_r[0, u], f"dV unit {u}")

@@ -136,3 +136,19 @@ def test_split_full_size_sampled():
     o_r, lse_r = oracle.fwd_rows_mod(q, k, v, w.softmax_scale, rows, -1, wr)
     assert_fwd_close(np64(o).reshape(-1, D)[rows], np64(lse).reshape(-1)[rows], o_r, lse_r,
                      "split prefill sampled")
+
+
+@pytest.mark.parametrize("wr", [-1, 4999], ids=["none", "bottom_right_causal"])
+def test_split_decode_rows(wr):
+    """One query per head (decode) against a 5000-key context, GQA 4, the
+    automatic split count."""
+    B, Hq, Hkv, Sq, Sk, D = 4, 8, 2, 1, 5000, 128
+    w = synth.Workload("split_decode", B, Hq, Hkv, Sq, Sk, D, False, 21)
+    q, k, v = synth.make_inputs(w)
+    n = fa.fwd_split_count(B, Hq, Sq, Sk)
+    assert n > 1
+    o, lse = fa.fwd(q.to(DEV), k.to(DEV), v.to(DEV), window=(-1, wr), n_splits=0)
+    torch.cuda.synchronize()
+    assert fa.fwd_status() == fa.FA_OK
+    o_r, lse_r = oracle.fwd_mod(q, k, v, w.softmax_scale, -1, wr)
+    assert_fwd_close(o, lse, o_r, lse_r, f"decode n={n}")
