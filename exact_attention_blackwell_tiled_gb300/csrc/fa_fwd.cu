@@ -595,49 +595,111 @@ __global__ void __launch_bounds__(320, 1)
         // this split (l = 0) is an empty part, O = 0 and LSE = -inf
         const bool empty = !(l_run > 0.f);
         const float inv = empty ? 0.f : 1.0f / l_run;
-        float* prow = a.o_part + (row_ok ? part_row : 0) * D;
+        // rows grp_row0 .. +3 of the lane group trade 16-byte pieces as in the
+        // bf16 epilogue below, in two rounds of four pieces
+        const int grp_row0 = qt * kTile + (r & ~3), pc = lane & 3;
+        float* pbase = a.o_part + (part_row - (size_t)(r & 3)) * D;  // the group's first row
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           __syncwarp();
           tmem_ld32(t_row + col_o + c * 32, v);
-          if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarOFree + t));
+          }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(u2f(v[4 * i]) * inv, u2f(v[4 * i + 1]) * inv,
-                                   u2f(v[4 * i + 2]) * inv, u2f(v[4 * i + 3]) * inv);
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(u2f(v[i]) * inv);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+              uint32_t x[4] = {v[16 * hf + wd], v[16 * hf + 4 + wd], v[16 * hf + 8 + wd],
+                               v[16 * hf + 12 + wd]};
+              xpose4(x, lane);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) v[16 * hf + 4 * m + wd] = x[m];
+            }
+            // v[16hf + 4m .. +3] is now piece 4hf + pc of row grp_row0 + m
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              if (grp_row0 + m < a.Sq)
+                *reinterpret_cast<uint4*>(pbase + (size_t)m * D + c * 32 + (4 * hf + pc) * 4) =
+                    make_uint4(v[16 * hf + 4 * m], v[16 * hf + 4 * m + 1], v[16 * hf + 4 * m + 2],
+                               v[16 * hf + 4 * m + 3]);
+            }
           }
         }
         if (row_ok)
           a.lse_part[part_row] =
               empty ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994531f;
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarOFree + t));
         continue;
       }
       const float inv_l = 1.0f / l_run;
-      __nv_bfloat16* orow =
-          reinterpret_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.Sq + (row_ok ? q_row : 0)) * D;
+      if constexpr (D == 128) {
+        // Each thread holds one row; so that a store instruction writes whole
+        // 64-byte row pieces instead of 16 bytes of 32 rows, the four lanes of
+        // a group trade 16-byte pieces (a 4x4 transpose): lane 4k+i then writes
+        // piece i of rows 4k..4k+3.  O is released after its last TMEM read.
+        const int grp_row0 = qt * kTile + (r & ~3), pc = lane & 3;
+        __nv_bfloat16* obase = reinterpret_cast<__nv_bfloat16*>(a.o) + (size_t)bh * a.Sq * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        __syncwarp();  // reconverge after the per-row store before the warp-wide load
-        tmem_ld32(t_row + col_o + c * 32, v);
-        uint32_t w[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          __syncwarp();  // reconverge after the per-row stores before the warp-wide load
+          tmem_ld32(t_row + col_o + c * 32, v);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarOFree + t));
+          }
+          uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(u2f(v[2 * i]) * inv_l, u2f(v[2 * i + 1]) * inv_l);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(u2f(v[2 * i]) * inv_l, u2f(v[2 * i + 1]) * inv_l);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int wd = 0; wd < 4; ++wd) {  // word wd of each 16-byte piece
+            uint32_t x[4] = {w[wd], w[4 + wd], w[8 + wd], w[12 + wd]};
+            xpose4(x, lane);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) w[4 * m + wd] = x[m];
+          }
+          // w[4m..4m+3] is now piece pc of row grp_row0 + m
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            if (grp_row0 + m < a.Sq)
+              *reinterpret_cast<uint4*>(obase + (size_t)(grp_row0 + m) * D + c * 32 + pc * 8) =
+                  make_uint4(w[4 * m], w[4 * m + 1], w[4 * m + 2], w[4 * m + 3]);
+          }
         }
+        if (row_ok)
+          a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      } else {
+        // D = 64: each thread stores its own row, and O is released after the
+        // stores (both measured faster here than the D = 128 form, whose
+        // shuffles cost the softmax-bound loop more than they save)
+        __nv_bfloat16* orow =
+            reinterpret_cast<__nv_bfloat16*>(a.o) + ((size_t)bh * a.Sq + (row_ok ? q_row : 0)) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          __syncwarp();  // reconverge after the per-row store before the warp-wide load
+          tmem_ld32(t_row + col_o + c * 32, v);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(u2f(v[2 * i]) * inv_l, u2f(v[2 * i + 1]) * inv_l);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        if (row_ok)
+          a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarOFree + t));
       }
-      if (row_ok) a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarOFree + t));
     }
   }
 

@@ -310,6 +310,28 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// ------------------------------------------------------------------ lane groups
+
+// 4x4 transpose of 32-bit values within the lane group (lane & ~3) .. +3: on
+// return v[m] holds what lane (lane & ~3) + m held in v[lane & 3].
+__device__ __forceinline__ void xpose4(uint32_t (&v)[4], int lane) {
+#pragma unroll
+  for (int mask = 1; mask < 4; mask <<= 1) {
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s & mask) continue;
+      const int s2 = s | mask;
+      const uint32_t send = upper ? v[s] : v[s2];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, mask);
+      if (upper)
+        v[s] = recv;
+      else
+        v[s2] = recv;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ arithmetic
 
 __device__ __forceinline__ float ex2_mufu(float x) {
