@@ -89,7 +89,7 @@ def test_split_close_to_unsplit():
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("n", [1, 3, 40])
+@pytest.mark.parametrize("n", [1, 3, 12, 25, 40])
 def test_lse_merge(n, D):
     """fa_lse_merge on random parts with empty parts (-inf, O rows NaN-filled to
     show they are not read) and rows whose parts are all empty."""
