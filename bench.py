@@ -281,6 +281,22 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in kev]
     bwd_main_ms = [e[2].elapsed_time(e[3]) for e in kev]
+    # the deterministic backward (semaphore-ordered dQ adds), main kernel only
+    ws_det = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True),
+                         dtype=torch.uint8, device=dev)
+    det_ms = []
+    for i in range(min(args.steps, 50) + 3):
+        flush.zero_()
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        fa.set_timing_events(*e)
+        fa.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=scale, workspace=ws_det, dq=dq,
+               dk=dk, dv=dv, deterministic=True)
+        if i >= 3:
+            det_ms.append(e)
+    torch.cuda.synchronize(dev)
+    assert fa.bwd_status(ws_det) == fa.FA_OK
+    det_ms = [a.elapsed_time(b) for a, b in det_ms]
+    del ws_det
     total_ms_local = sum(step_ms)
     total_ms = max_over_ranks(total_ms_local, world, dev)
     ms_per_step = total_ms / args.steps
@@ -377,6 +393,8 @@ def run_ours(args):
 
     extra = {"fwd_tflops": round(fwd_tf, 1), "fwd_ms": round(fwd_avg, 4),
              "bwd_main_tflops": round(bwd_tf, 1), "bwd_main_ms": round(bwd_avg, 4),
+             "bwd_main_det_tflops": round(bwd_f / (sum(det_ms) / len(det_ms) * 1e-3) / 1e12, 1),
+             "det_over_atomic": round(bwd_avg / (sum(det_ms) / len(det_ms)), 3),
              "bwd_total_flops_tflops_incl_pre_post": None,
              "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak,
              # the vendor's dense bf16 figure for one GB300 (2.25 PFLOP/s without
