@@ -142,17 +142,18 @@ bool make_tmap_bsd(CUtensorMap* map, const void* base, int BH, int S, int D, int
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-bool bwd_layout(int B, int Hq, int Sq, int D, BwdLayout* L) {
+bool bwd_layout(int B, int Hq, int Sq, int D, int groups, BwdLayout* L) {
   // A 256-byte header holding the status word comes first, so fa_bwd_status can
   // find it without knowing the sizes.
   const size_t nq = (size_t)((Sq + kTile - 1) / kTile);
   const size_t rows = (size_t)B * Hq * nq * kTile;
   L->off_status = 0;
   L->off_dq_acc = 256;
-  L->off_delta = align256(L->off_dq_acc + rows * D * sizeof(float));
+  L->off_delta = align256(L->off_dq_acc + (size_t)groups * rows * D * sizeof(float));
   L->off_lse2 = align256(L->off_delta + rows * sizeof(float));
   L->off_sem = align256(L->off_lse2 + rows * sizeof(float));
-  L->total = align256(L->off_sem + (size_t)B * Hq * (2 * nq > 0 ? 2 * nq : 1) * sizeof(int));
+  L->total = align256(L->off_sem +
+                      (size_t)groups * B * Hq * (2 * nq > 0 ? 2 * nq : 1) * sizeof(int));
   return true;
 }
 
@@ -379,10 +380,9 @@ int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void
 }
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
-  (void)deterministic;
   if (check_shape(B, Hq, Hkv, Sq, Sk, D, 1.0f) != FA_OK) return 0;
   BwdLayout L;
-  bwd_layout(B, Hq, Sq, D, &L);
+  bwd_layout(B, Hq, Sq, D, dq_group_count(Sk, deterministic), &L);
   return L.total;
 }
 
@@ -410,7 +410,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
                 !aligned16(dq)))
     return FA_ERR_MISALIGNED;
   BwdLayout L;
-  bwd_layout(B, Hq, Sq, D, &L);
+  const int groups = dq_group_count(Sk, deterministic);
+  bwd_layout(B, Hq, Sq, D, groups, &L);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < L.total)
     return FA_ERR_WORKSPACE;
@@ -459,6 +460,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // (q, dO) fit comfortably in L2
   a.snake = (a.causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
   a.deterministic = deterministic ? 1 : 0;
+  a.dq_groups = groups;
+  a.dq_group_stride = (size_t)B * Hq * a.Sq_pad * D;
+  a.sem_group_stride = B * Hq * a.n_qblk;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));

@@ -153,13 +153,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const BwdArgs a) {
           a.delta[r] = acc;
           a.lse2[r] = real[u] ? a.lse[(size_t)bh * a.Sq + i] * 1.4426950408889634f : INFINITY;
         }
-        float4* dqa = reinterpret_cast<float4*>(a.dq_acc + (size_t)r * D + seg * 8);
-        dqa[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dqa[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.dq_groups == 1 && !a.deterministic) {
+          // the atomic mode adds into a cleared accumulator; the deterministic
+          // mode's first contributor of each group stores instead
+          float4* dqa = reinterpret_cast<float4*>(a.dq_acc + (size_t)r * D + seg * 8);
+          dqa[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          dqa[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
   }
-  const long long nsem = (long long)a.B * a.Hq * a.n_qblk;
+  const long long nsem = (long long)a.dq_groups * a.sem_group_stride;
   for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < nsem;
        s += (long long)gridDim.x * blockDim.x)
     a.sem[s] = 0;
@@ -232,13 +236,17 @@ __device__ __forceinline__ void bwd_qblk_range(const BwdArgs& a, int j, int& lo,
   hi = q_hi >= q_lo ? q_hi / kQB + 1 : lo;
 }
 
-// First kv tile whose keys a query of block iq sees (the smallest tile whose
-// last key reaches the block's first query minus wl); the tiles that add into
-// block iq are those from it on, as bwd_qblk_range lists them.
-template <bool kMod>
-__device__ __forceinline__ int bwd_ktile_first(const BwdArgs& a, int iq) {
-  const int wl = win_left<kMod>(a);
-  return wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
+// The kv tiles [first, last] that add into 64-row query block iq under the
+// window (wl, wr): those whose query-block range (bwd_qblk_range) holds iq.
+__device__ __forceinline__ void qblk_contributors(const BwdArgs& a, int wl, int wr, int iq,
+                                                  int& first, int& last) {
+  first = wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
+  last = wr >= 0 ? min(a.n_ktiles - 1, (iq * kQB + kQB - 1 + wr) / kTile) : a.n_ktiles - 1;
+}
+
+// The first kv tile >= first that belongs to deterministic group g.
+__device__ __forceinline__ int group_first(int first, int g, int groups) {
+  return first + ((g - first % groups) % groups + groups) % groups;
 }
 
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -760,51 +768,82 @@ __global__ void __launch_bounds__(BwdRoles<kMod>::kThreads, 1)
         // Row r of dQ^T (head-dim index r, 64 queries) goes straight from TMEM
         // to the fp32 accumulator: for each query the 32 lanes of a warp add
         // 32 consecutive floats, one 128-byte line per instruction.
-        float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
         constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
-        if (a.deterministic && wq < kAddWarps) {
-          // kv tiles add into block iq in ascending order: the semaphore counts
-          // finished adding warps, so tile j starts once every tile from the
-          // block's first contributor on has added (j - j_first) * kAddWarps
-          int* sem = a.sem + (size_t)bh * a.n_qblk + iq;
-          if (lane == 0) {
-            const uint64_t t0 = global_timer_ns();
-            const int j_first = bwd_ktile_first<kMod>(a, iq);
-            while (ld_acquire(sem) < (w.j - j_first) * kAddWarps) {
-              if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
-                *abort_flag = 1;
-                good = 0;
-                break;
+        if (!a.deterministic) {
+          // two 32-column halves, so that only 32 values are live at a time;
+          // the columns are released once the second half is read
+          float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[32];
+            tmem_ld32(t_row + L::kColDQ + hf * 32, v);
+            if (hf == 1) {
+              tc_fence_before();
+              mbar_arrive(bar(L::kBarDQEmpty));
+            }
+            if (r < D) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(
+                                 dst + (size_t)(hf * 32 + e) * D),
+                             "f"(u2f(v[e]))
+                             : "memory");
+            }
+          }
+        } else {
+          // deterministic mode: kv tile j adds into accumulator g = j % G after
+          // the tiles of its group before it (from the block's first
+          // contributor on); the first of them stores instead of adding
+          int first, last;
+          qblk_contributors(a, win_left<kMod>(a), win_right<kMod>(a), iq, first, last);
+          const int g = w.j % a.dq_groups;
+          const int turn = (w.j - group_first(first, g, a.dq_groups)) / a.dq_groups;
+          float* dst = a.dq_acc + (size_t)g * a.dq_group_stride +
+                       ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
+          int* sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;
+          if (wq < kAddWarps && turn > 0) {
+            // the semaphore counts the group's finished adding warps
+            if (lane == 0) {
+              const uint64_t t0 = global_timer_ns();
+              while (ld_acquire(sem) < turn * kAddWarps) {
+                if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
+                  *abort_flag = 1;
+                  good = 0;
+                  break;
+                }
+              }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[32];
+            tmem_ld32(t_row + L::kColDQ + hf * 32, v);
+            if (hf == 1) {
+              tc_fence_before();
+              mbar_arrive(bar(L::kBarDQEmpty));
+            }
+            if (good && r < D) {
+              if (turn == 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dst[(size_t)(hf * 32 + e) * D] = u2f(v[e]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(
+                                   dst + (size_t)(hf * 32 + e) * D),
+                               "f"(u2f(v[e]))
+                               : "memory");
               }
             }
           }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          __syncwarp();
-        }
-        // two 32-column halves, so that only 32 values are live at a time; the
-        // columns are released once the second half is read
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v[32];
-          tmem_ld32(t_row + L::kColDQ + hf * 32, v);
-          if (hf == 1) {
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarDQEmpty));
+          if (wq < kAddWarps && good) {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(sem, 1);
           }
-          if (good && r < D) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(
-                               dst + (size_t)(hf * 32 + e) * D),
-                           "f"(u2f(v[e]))
-                           : "memory");
-          }
-        }
-        if (a.deterministic && wq < kAddWarps && good) {
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) atomicAdd(a.sem + (size_t)bh * a.n_qblk + iq, 1);
         }
         ok = group_all(good != 0, 2);
         if (!ok) break;
@@ -889,9 +928,23 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
     const uint32_t c8 = (uint32_t)(x - (uint64_t)row * kPerRow);
     const uint32_t bh = row / (uint32_t)a.Sq;
     const uint32_t i = row - bh * (uint32_t)a.Sq;
-    const float4* src =
-        reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Sq_pad + i) * D + c8 * 8);
-    const float4 x0 = src[0], x1 = src[1];
+    const float* base = a.dq_acc + ((size_t)bh * a.Sq_pad + i) * D + c8 * 8;
+    float4 x0 = reinterpret_cast<const float4*>(base)[0];
+    float4 x1 = reinterpret_cast<const float4*>(base)[1];
+    if (a.deterministic) {
+      // the groups' accumulators in fixed order; a group with no contributing
+      // kv tile for this query block was never written
+      int first, last;
+      qblk_contributors(a, a.wl, a.wr, (int)(i / kQB), first, last);
+      if (group_first(first, 0, a.dq_groups) > last) x0 = x1 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int g = 1; g < a.dq_groups; ++g) {
+        if (group_first(first, g, a.dq_groups) > last) continue;
+        const float4* src = reinterpret_cast<const float4*>(base + (size_t)g * a.dq_group_stride);
+        const float4 y0 = src[0], y1 = src[1];
+        x0.x += y0.x, x0.y += y0.y, x0.z += y0.z, x0.w += y0.w;
+        x1.x += y1.x, x1.y += y1.y, x1.z += y1.z, x1.w += y1.w;
+      }
+    }
     uint4 w;
     w.x = pack_bf16x2(x0.x * a.scale, x0.y * a.scale);
     w.y = pack_bf16x2(x0.z * a.scale, x0.w * a.scale);

@@ -78,10 +78,10 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;   // [B, Hq, Sq_pad, D]
+  float* dq_acc;   // dq_groups x [B, Hq, Sq_pad, D]
   float* delta;    // [B, Hq, Sq_pad]
   float* lse2;     // [B, Hq, Sq_pad]
-  int* sem;        // [B, Hq, n_qblk]
+  int* sem;        // dq_groups x [B, Hq, n_qblk]
   int* status;     // [1]
   int B, Hq, Hkv, Sq, Sk, D;
   int Sq_pad;
@@ -97,12 +97,25 @@ struct BwdArgs {
   int n_ktiles;  // 128-row kv tiles of Sk
   int n_units;
   int snake;     // 1: units dealt longest-first (ascending kv tile) in a snake
+  // dQ accumulators: 1 in the atomic mode; in the deterministic mode kv tile j
+  // adds into accumulator j % dq_groups, chained only behind tile j - dq_groups
+  int dq_groups;
+  size_t dq_group_stride;  // floats from one accumulator to the next
+  int sem_group_stride;    // semaphores from one group to the next
 };
+
+constexpr int kDetGroups = 4;  // deterministic-mode accumulators (at most)
+
+// Accumulators of a backward call: 1 atomic, else min(kDetGroups, kv tiles).
+inline int dq_group_count(int Sk, int deterministic) {
+  const int n_ktiles = (Sk + kTile - 1) / kTile;
+  return deterministic ? (n_ktiles < kDetGroups ? (n_ktiles > 0 ? n_ktiles : 1) : kDetGroups) : 1;
+}
 
 struct BwdLayout {
   size_t off_dq_acc, off_delta, off_lse2, off_sem, off_status, total;
 };
-bool bwd_layout(int B, int Hq, int Sq, int D, BwdLayout* L);
+bool bwd_layout(int B, int Hq, int Sq, int D, int groups, BwdLayout* L);
 
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);

@@ -108,10 +108,14 @@ int fa_fwd_status(fa_stream_t stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for these sizes (0 on bad sizes).  The
- * workspace holds an fp32 dQ accumulator [B, Hq, ceil(Sq/128)*128, D], the
- * per-row dot products D_i = dO_i . O_i and LSE*log2(e) (fp32 [B, Hq, padded
- * Sq]), the deterministic mode's per-(b, h, 64-row query block) semaphores and
- * a status word.  It needs no initialisation: fa_bwd clears what it uses.
+ * workspace holds fp32 dQ accumulators [B, Hq, ceil(Sq/128)*128, D] (one in the
+ * atomic mode; in the deterministic mode min(4, ceil(Sk/128)), kv tile j adding
+ * into accumulator j % 4 in its own ordered chain, the accumulators summed in
+ * fixed order at the end), the per-row dot products D_i = dO_i . O_i and
+ * LSE*log2(e) (fp32 [B, Hq, padded Sq]), the deterministic mode's per-(group,
+ * b, h, 64-row query block) semaphores and a status word.  The deterministic
+ * size is at least the atomic one.  It needs no initialisation: fa_bwd clears
+ * or overwrites what it uses.
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
 
