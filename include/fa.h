@@ -256,7 +256,8 @@ int fa_set_timing_events(void* start_event, void* stop_event);
  * until the process exits.  No call allocates or frees memory.
  *   - Sizes whose workspace (fa_bwd_workspace_bytes) exceeds 32 MiB are
  *     rejected with FA_ERR_WORKSPACE (about 64,000 query rows B*Hq*Sq at
- *     D = 128, about 127,000 at D = 64); invalid sizes return
+ *     D = 128, about 127,000 at D = 64; in the deterministic mode, which keeps up
+ *     to four accumulators, about a quarter of those); invalid sizes return
  *     FA_ERR_INVALID_ARG.
  *   - The first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
