@@ -840,9 +840,11 @@ __global__ void __launch_bounds__(BwdRoles<kMod>::kThreads, 1)
             }
           }
           if (wq < kAddWarps && good) {
-            __threadfence();
+            // the warp barrier orders every lane's adds before lane 0's
+            // release, which makes them visible before the count moves
             __syncwarp();
-            if (lane == 0) atomicAdd(sem, 1);
+            if (lane == 0)
+              asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
           }
         }
         ok = group_all(good != 0, 2);
