@@ -8,8 +8,8 @@
 // reductions through semaphores).
 //
 //   1. bwd_preprocess  Delta_i = sum_d dO_id O_id and LSE*log2(e) (+inf on padded
-//                      rows); clears the fp32 dQ accumulator, the semaphores and
-//                      the status word.
+//                      rows); clears the semaphores, the status word and (in
+//                      the atomic mode) the fp32 dQ accumulator.
 //   2. bwd_main        persistent over (batch, kv head, 128-row kv tile j).  K_j
 //                      and V_j stay in shared memory; for every q head of the
 //                      group and every 64-row query block i that can see tile j:
@@ -24,11 +24,13 @@
 //                      of the 64 query rows, so every warp instruction covers
 //                      one 128-byte line (no shared-memory staging, which would
 //                      compete with the MMA operand reads for shared-memory
-//                      bandwidth).  In the deterministic mode each warp adds in
-//                      kv-tile order behind a per-(b, h, block) semaphore.  At
-//                      the end of the unit dK_j * scale and dV_j are written as
-//                      bf16.
-//   3. bwd_dq_convert  dQ = scale * accumulator -> bf16.
+//                      bandwidth).  In the deterministic mode kv tile j adds
+//                      into accumulator j % G (G <= 4), in kv-tile order within
+//                      its group behind a per-(group, b, h, block) semaphore;
+//                      the group's first contributor stores.  At the end of the
+//                      unit dK_j * scale and dV_j are written as bf16.
+//   3. bwd_dq_convert  dQ = scale * accumulator -> bf16 (deterministic mode: the
+//                      sum of the groups' accumulators in fixed order).
 //
 // bwd_main warp roles, with n = 8 softmax warps (plain kernel: 512 threads,
 // 128 registers) or n = 16 (score-modified kernel: 768 threads, 80 registers):
