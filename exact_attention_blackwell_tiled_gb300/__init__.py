@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa.so")
 
 FA_OK = 0
+FA_ERR_TIMEOUT = 6
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA",
                 6: "FA_ERR_TIMEOUT"}
@@ -26,7 +27,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
            "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
            "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod", "fa_fwd_split_count",
-           "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge")
+           "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge", "fa_wait_test")
 
 
 class ScoreMod(ctypes.Structure):
@@ -83,6 +84,8 @@ def _bind(lib):
     lib.fa_fwd_split.restype = i
     lib.fa_lse_merge.argtypes = [vp, vp, i, vp, vp, i64, i, vp]
     lib.fa_lse_merge.restype = i
+    lib.fa_wait_test.argtypes = [vp, i, vp, vp]
+    lib.fa_wait_test.restype = i
     return lib
 
 
@@ -278,6 +281,18 @@ def exp2_test(x: torch.Tensor, which: int, stream=None) -> torch.Tensor:
     if rc != FA_OK:
         raise FAError("fa_exp2_test", rc)
     return y
+
+
+def wait_test(which: int, flag: torch.Tensor | None = None, stream=None) -> int:
+    """Run one of the kernels' bounded waits (fa_wait_test); returns the status it
+    wrote: FA_OK or FA_ERR_TIMEOUT (6).  flag: an int32 CUDA scalar for which=0."""
+    status = torch.full((1,), -1, dtype=torch.int32, device=flag.device if flag is not None
+                        else torch.device("cuda", torch.cuda.current_device()))
+    rc = lib().fa_wait_test(None if flag is None else _ptr(flag), int(which), _ptr(status),
+                            _stream(stream))
+    if rc != FA_OK:
+        raise FAError("fa_wait_test", rc)
+    return int(status.item())
 
 
 def last_launch_count() -> int:

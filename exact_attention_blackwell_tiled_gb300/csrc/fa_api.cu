@@ -498,6 +498,16 @@ int fa_bwd_status(const void* workspace, fa_stream_t stream) {
   return v == 0 ? FA_OK : v;
 }
 
+int fa_wait_test(const int* flag, int which, int* status, fa_stream_t stream) {
+  t_launches = 0;
+  if (which < 0 || which > 1 || !status || (which == 0 && !flag)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(status) & 3) || (flag && (reinterpret_cast<uintptr_t>(flag) & 3)))
+    return FA_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_wait_test(flag, which, status, static_cast<cudaStream_t>(stream));
+}
+
 int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream) {
   t_launches = 0;
   if (n < 0 || which < 0 || which > 2) return FA_ERR_INVALID_ARG;

@@ -1037,4 +1037,42 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   return FA_ERR_UNSUPPORTED;
 }
 
+// ------------------------------------------------------------------ wait test hook
+
+// One thread runs one of the kernels' bounded waits on something that may
+// never happen, and writes FA_OK or FA_ERR_TIMEOUT to *status.
+//   which 0: the deterministic mode's semaphore spin, on *flag reaching 1;
+//   which 1: an mbarrier wait on a phase that nothing completes.
+__global__ void wait_test_kernel(const int* flag, int which, int* status) {
+  __shared__ uint64_t mbar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    abort_word = 0;
+    mbar_init(smem_u32(&mbar), 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  bool ok = true;
+  if (which == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire(flag) < 1) {
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        ok = false;
+        break;
+      }
+    }
+  } else {
+    ok = mbar_wait(smem_u32(&mbar), 0, &abort_word);
+  }
+  *status = ok ? (int)FA_OK : (int)FA_ERR_TIMEOUT;
+}
+
+int launch_wait_test(const int* flag, int which, int* status, cudaStream_t stream) {
+  wait_test_kernel<<<1, 32, 0, stream>>>(flag, which, status);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  note_launches(1);
+  return FA_OK;
+}
+
 }  // namespace fa

@@ -70,6 +70,7 @@ struct MergeArgs {
 int launch_merge(const MergeArgs& m, int D, cudaStream_t stream);
 int fwd_status_take(cudaStream_t stream);
 int launch_exp2_test(const float* x, float* y, int64_t n, int which, cudaStream_t stream);
+int launch_wait_test(const int* flag, int which, int* status, cudaStream_t stream);
 
 struct BwdArgs {
   const void* o;

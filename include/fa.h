@@ -231,6 +231,20 @@ const char* fa_status_string(int status);
  */
 int fa_exp2_test(const float* x, float* y, int64_t n, int which, fa_stream_t stream);
 
+/*
+ * Test hook for the kernels' bounded waits.  One device thread runs one of the
+ * waits the kernels use, with the same time limit (2 s of the GPU's global
+ * timer), and writes FA_OK or FA_ERR_TIMEOUT to the device int *status:
+ *   which = 0: the deterministic backward's semaphore spin, until the device
+ *              int *flag reaches 1;
+ *   which = 1: an mbarrier wait on a phase that nothing completes (always
+ *              FA_ERR_TIMEOUT; flag is unused and may be null).
+ * Returns FA_ERR_INVALID_ARG for another `which` or a null pointer it needs,
+ * FA_ERR_MISALIGNED for pointers not 4-byte aligned; otherwise the launch
+ * status.  The wait running out leaves the CUDA context usable.
+ */
+int fa_wait_test(const int* flag, int which, int* status, fa_stream_t stream);
+
 /* Number of kernels the last forward, backward or merge call on this thread
  * launched. */
 int fa_last_launch_count(void);

@@ -171,6 +171,14 @@ def test_merge_validation(L):
     assert merge(lp=ctypes.c_void_p(16 * 1024 + 2)) == 3
 
 
+def test_wait_hook_validation(L):
+    assert L.fa_wait_test(P16, 2, P16, None) == 1    # unknown wait
+    assert L.fa_wait_test(None, 0, P16, None) == 1   # the semaphore wait needs its flag
+    assert L.fa_wait_test(P16, 0, None, None) == 1   # no status word
+    assert L.fa_wait_test(ctypes.c_void_p(16 * 1024 + 2), 0, P16, None) == 3
+    assert L.fa_wait_test(None, 1, ctypes.c_void_p(16 * 1024 + 1), None) == 3
+
+
 def test_exp2_hook_validation(L):
     assert L.fa_exp2_test(None, None, 0, 0, None) == 0
     assert L.fa_exp2_test(None, None, -1, 0, None) == 1
