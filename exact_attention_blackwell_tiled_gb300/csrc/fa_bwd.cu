@@ -32,8 +32,9 @@
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16 (deterministic mode: the
 //                      sum of the groups' accumulators in fixed order).
 //
-// bwd_main warp roles, with n = 8 softmax warps (plain kernel: 512 threads,
-// 128 registers) or n = 16 (score-modified kernel: 768 threads, 80 registers):
+// bwd_main warp roles, with n = 8 softmax warps (plain D = 128 kernel: 512
+// threads, 128 registers) or n = 16 (score-modified and D = 64 kernels: 768
+// threads, 80 registers):
 //   warps 0..n-1  P^T / dS^T: warp w serves key rows 32*(w%4).. (its TMEM
 //                 lanes) and query columns c*(w/4).. of the block, c = 4*64/n
 //                 (32 or 16), so each SM sub-partition runs n/4 of them and
@@ -77,12 +78,13 @@ namespace fa {
 constexpr int kQB = 64;  // query rows per backward block
 
 // bwd_main warp roles.  The score-modified kernel (masks, bias: more softmax
-// work per score) runs 16 softmax warps of 16 query columns each, 768 threads
-// at 80 registers; the plain kernel 8 of 32 columns, 512 threads at 128
-// registers, which measured faster there.
-template <bool kMod>
+// work per score) and the D = 64 kernels (half the tensor work per score) run
+// 16 softmax warps of 16 query columns each, 768 threads at 80 registers; the
+// plain D = 128 kernel 8 of 32 columns, 512 threads at 128 registers, which
+// measured faster there.
+template <bool kWide>
 struct BwdRoles {
-  static constexpr int kSmxWarps = kMod ? 16 : 8;  // warps 0..: P^T / dS^T
+  static constexpr int kSmxWarps = kWide ? 16 : 8;  // warps 0..: P^T / dS^T
   static constexpr int kSmxCols = 4 * kQB / kSmxWarps;  // query columns per softmax warp
   static constexpr int kDrainWarp0 = kSmxWarps;    // 4 warps: dQ drain, dK/dV epilogue
   static constexpr int kTmaWarp = kDrainWarp0 + 4;
@@ -384,12 +386,12 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
 // plain kernel applies no mask or the causal one.
 template <int D, bool kMod>
-__global__ void __launch_bounds__(BwdRoles<kMod>::kThreads, 1)
+__global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
   using L = BwdSmem<D>;
-  using R = BwdRoles<kMod>;
+  using R = BwdRoles<kMod || D == 64>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -992,7 +994,8 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     // a window other than none / causal, or a bias, selects the general kernel
     const bool mod = a.alibi || !(a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal)));
     const auto kernel = mod ? bwd_main<D, true> : bwd_main<D, false>;
-    const int threads = mod ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;
+    const int threads =
+        (mod || D == 64) ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;
     record_timing(false, stream);
     if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
