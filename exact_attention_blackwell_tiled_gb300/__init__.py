@@ -310,3 +310,35 @@ def set_timing_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event 
     rc = lib().fa_set_timing_events(ps, pe)
     if rc != FA_OK:
         raise FAError("fa_set_timing_events", rc)
+
+
+class _Attention(torch.autograd.Function):
+    """fwd in forward (saving O and LSE), bwd in backward; nothing else runs."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, window, alibi_slopes, deterministic):
+        o, lse = fwd(q, k, v, causal=causal, scale=scale, window=window,
+                     alibi_slopes=alibi_slopes)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.args = (causal, scale, window, alibi_slopes, deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        causal, scale, window, alibi_slopes, deterministic = ctx.args
+        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, causal=causal, scale=scale,
+                         deterministic=deterministic, window=window, alibi_slopes=alibi_slopes)
+        return dq, dk, dv, None, None, None, None, None
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+              scale: float | None = None, window=None, alibi_slopes=None,
+              deterministic: bool = False) -> torch.Tensor:
+    """Exact attention as a differentiable op: O = softmax(scale q k^T + mods) v.
+
+    q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA; ``causal``, ``window`` and
+    ``alibi_slopes`` as in fwd; ``deterministic`` selects the backward mode.
+    O.backward() runs fa_bwd (the slopes get no gradient).  Returns O bf16.
+    """
+    return _Attention.apply(q, k, v, causal, scale, window, alibi_slopes, deterministic)
