@@ -37,15 +37,15 @@ def _bind(lib):
     lib.oracle_bwd_units.argtypes = [p, p, p, p, i, i, i, i, i, i, i, d, p, ctypes.c_int64,
                                      p, p, p, p, p]
     lib.oracle_bwd_units.restype = i
-    lib.oracle_fwd_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, p]
+    lib.oracle_fwd_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, p, p]
     lib.oracle_fwd_mod.restype = i
-    lib.oracle_fwd_rows_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, ctypes.c_int64,
-                                        p, p]
+    lib.oracle_fwd_rows_mod.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, p,
+                                        ctypes.c_int64, p, p]
     lib.oracle_fwd_rows_mod.restype = i
-    lib.oracle_bwd_units_mod.argtypes = [p, p, p, p, i, i, i, i, i, i, d, i, i, p, p,
+    lib.oracle_bwd_units_mod.argtypes = [p, p, p, p, i, i, i, i, i, i, d, i, i, p, p, p,
                                          ctypes.c_int64, p, p, p, p, p]
     lib.oracle_bwd_units_mod.restype = i
-    lib.oracle_fwd_mod_range.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, i, i, p, p]
+    lib.oracle_fwd_mod_range.argtypes = [p, p, p, i, i, i, i, i, i, d, i, i, p, p, i, i, p, p]
     lib.oracle_fwd_mod_range.restype = i
     lib.oracle_lse_merge.argtypes = [p, p, i, ctypes.c_long, i, p, p]
     lib.oracle_lse_merge.restype = i
@@ -145,6 +145,17 @@ def bwd(q, k, v, do, causal: bool, scale: float, units=None, lib=None):
     return dq, dk, dv, o, lse
 
 
+def _seqlens(seqlens_k, B):
+    """Per-batch key lengths as a contiguous int32 array (None: all keys)."""
+    if seqlens_k is None:
+        return None
+    if hasattr(seqlens_k, "detach"):
+        seqlens_k = seqlens_k.detach().to("cpu").numpy()
+    a = np.ascontiguousarray(np.asarray(seqlens_k, dtype=np.int32).reshape(-1))
+    assert a.shape == (B,), "one key length per batch"
+    return a
+
+
 def _slopes(slopes, Hq):
     if slopes is None:
         return None
@@ -154,37 +165,43 @@ def _slopes(slopes, Hq):
 
 
 def fwd_mod(q, k, v, scale: float, window_left: int = -1, window_right: int = -1, slopes=None,
-            lib=None):
+            seqlens_k=None, lib=None):
     """Forward with the score modification: key j visible to query i iff
     (window_left < 0 or j >= i - window_left) and (window_right < 0 or
-    j <= i + window_right); score scale*q.k + slopes[h]*(j - i).  Returns (O, LSE)."""
+    j <= i + window_right) and j < seqlens_k[b]; score scale*q.k +
+    slopes[h]*(j - i).  Returns (O, LSE); a row with no visible key has O = 0,
+    LSE = -inf."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
     sl = _slopes(slopes, Hq)
+    sk = _seqlens(seqlens_k, B)
     o = np.zeros((B, Hq, Sq, D))
     lse = np.zeros((B, Hq, Sq))
     rc = lib.oracle_fwd_mod(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
                             int(window_left), int(window_right),
-                            None if sl is None else _ptr(sl), _ptr(o), _ptr(lse))
+                            None if sl is None else _ptr(sl), None if sk is None else _ptr(sk),
+                            _ptr(o), _ptr(lse))
     if rc:
         raise ValueError(f"oracle_fwd_mod rejected its arguments ({rc})")
     return o, lse
 
 
 def fwd_rows_mod(q, k, v, scale: float, rows, window_left: int = -1, window_right: int = -1,
-                 slopes=None, lib=None):
+                 slopes=None, seqlens_k=None, lib=None):
     """fwd_mod for selected flat rows (b*Hq + h)*Sq + i. Returns (O [n,D], LSE [n])."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
     sl = _slopes(slopes, Hq)
+    sk = _seqlens(seqlens_k, B)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     o = np.zeros((len(rows), D))
     lse = np.zeros(len(rows))
     rc = lib.oracle_fwd_rows_mod(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
                                  int(window_left), int(window_right),
-                                 None if sl is None else _ptr(sl), _ptr(rows), len(rows),
+                                 None if sl is None else _ptr(sl),
+                                 None if sk is None else _ptr(sk), _ptr(rows), len(rows),
                                  _ptr(o), _ptr(lse))
     if rc:
         raise ValueError(f"oracle_fwd_rows_mod rejected its arguments ({rc})")
@@ -192,12 +209,13 @@ def fwd_rows_mod(q, k, v, scale: float, rows, window_left: int = -1, window_righ
 
 
 def bwd_mod(q, k, v, do, scale: float, window_left: int = -1, window_right: int = -1,
-            slopes=None, units=None, lib=None):
+            slopes=None, units=None, seqlens_k=None, lib=None):
     """Backward with the score modification (see fwd_mod); same return as bwd."""
     lib = lib or load()
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
     sl = _slopes(slopes, Hq)
+    sk = _seqlens(seqlens_k, B)
     if units is None:
         units = np.arange(B * Hkv)
     units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
@@ -208,7 +226,8 @@ def bwd_mod(q, k, v, do, scale: float, window_left: int = -1, window_right: int 
     lse = np.full((B, Hq, Sq), np.nan)
     rc = lib.oracle_bwd_units_mod(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Sq, Sk, D,
                                   float(scale), int(window_left), int(window_right),
-                                  None if sl is None else _ptr(sl), _ptr(units), len(units),
+                                  None if sl is None else _ptr(sl),
+                                  None if sk is None else _ptr(sk), _ptr(units), len(units),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(o), _ptr(lse))
     if rc:
         raise ValueError(f"oracle_bwd_units_mod rejected its arguments ({rc})")
@@ -216,18 +235,20 @@ def bwd_mod(q, k, v, do, scale: float, window_left: int = -1, window_right: int 
 
 
 def fwd_mod_range(q, k, v, scale: float, k0: int, k1: int, window_left: int = -1,
-                  window_right: int = -1, slopes=None, lib=None):
+                  window_right: int = -1, slopes=None, seqlens_k=None, lib=None):
     """fwd_mod over the keys [k0, k1) only (window and bias at the absolute key
     index).  Rows with no visible key there get O = 0, LSE = -inf."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k)
     sl = _slopes(slopes, Hq)
+    sk = _seqlens(seqlens_k, B)
     o = np.zeros((B, Hq, Sq, D))
     lse = np.zeros((B, Hq, Sq))
     rc = lib.oracle_fwd_mod_range(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, float(scale),
                                   int(window_left), int(window_right),
-                                  None if sl is None else _ptr(sl), int(k0), int(k1), _ptr(o),
+                                  None if sl is None else _ptr(sl),
+                                  None if sk is None else _ptr(sk), int(k0), int(k1), _ptr(o),
                                   _ptr(lse))
     if rc:
         raise ValueError(f"oracle_fwd_mod_range rejected its arguments ({rc})")

@@ -284,8 +284,11 @@ int oracle_bwd_units(const double* q, const double* k, const double* v, const do
  * visible to query i iff (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr), so
  * wl = -1, wr = 0 is the causal mask and wl = wr = -1 no mask; the score of a
  * visible pair in query head h is scale * q_i . k_j + slope[h] * (j - i) (slopes
- * NULL: no bias).  The row's softmax, LSE and the gradients follow the plain
- * definition with that score.
+ * NULL: no bias).  A custom key padding mask: with per-batch key lengths
+ * seqlens_k (NULL: none), keys j >= seqlens_k[b] are invisible in batch b.  The
+ * row's softmax, LSE and the gradients follow the plain definition with that
+ * score over the visible keys; a row with none has O = 0 and LSE = -inf and
+ * contributes no gradient.
  */
 
 /* Visible keys of query i: the interval [*lo, *hi) (empty when *hi <= *lo). */
@@ -329,10 +332,18 @@ static void mod_fwd_row(const double* qi, const double* k_head, const double* v_
 
 static double head_slope(const double* slopes, long h) { return slopes ? slopes[h] : 0.0; }
 
+/* Keys of batch b that exist: the first seqlens_k[b] (clamped to [0, Sk]);
+ * all Sk without lengths.  Keys past it are invisible to every query. */
+static long batch_keys(const int* seqlens_k, long b, long Sk) {
+  if (!seqlens_k) return Sk;
+  const long L = seqlens_k[b];
+  return L < 0 ? 0 : (L > Sk ? Sk : L);
+}
+
 /* Full forward with the score modification: O [B,Hq,Sq,D], LSE [B,Hq,Sq]. */
 int oracle_fwd_mod(const double* q, const double* k, const double* v, int B, int Hq, int Hkv,
                    int Sq, int Sk, int D, double scale, int wl, int wr, const double* slopes,
-                   double* o, double* lse) {
+                   const int* seqlens_k, double* o, double* lse) {
   int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
   if (rc) return rc;
   const long total = (long)B * Hq * Sq;
@@ -345,7 +356,7 @@ int oracle_fwd_mod(const double* q, const double* k, const double* v, int B, int
       const long b = bh / Hq, h = bh % Hq;
       const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
       long lo, hi;
-      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      mod_key_range(i, batch_keys(seqlens_k, b, Sk), wl, wr, &lo, &hi);
       mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,
                   scale, head_slope(slopes, h), s, o + flat * D, lse + flat);
     }
@@ -357,8 +368,8 @@ int oracle_fwd_mod(const double* q, const double* k, const double* v, int B, int
 /* Forward with the score modification for selected flat rows (b*Hq + h)*Sq + i. */
 int oracle_fwd_rows_mod(const double* q, const double* k, const double* v, int B, int Hq,
                         int Hkv, int Sq, int Sk, int D, double scale, int wl, int wr,
-                        const double* slopes, const int64_t* rows, int64_t n_rows,
-                        double* o_rows, double* lse_rows) {
+                        const double* slopes, const int* seqlens_k, const int64_t* rows,
+                        int64_t n_rows, double* o_rows, double* lse_rows) {
   int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
   if (rc) return rc;
   const long total = (long)B * Hq * Sq;
@@ -374,7 +385,7 @@ int oracle_fwd_rows_mod(const double* q, const double* k, const double* v, int B
       const long b = bh / Hq, h = bh % Hq;
       const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
       long lo, hi;
-      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      mod_key_range(i, batch_keys(seqlens_k, b, Sk), wl, wr, &lo, &hi);
       mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,
                   scale, head_slope(slopes, h), s, o_rows + r * D, lse_rows + r);
     }
@@ -390,8 +401,9 @@ int oracle_fwd_rows_mod(const double* q, const double* k, const double* v, int B
  */
 int oracle_bwd_units_mod(const double* q, const double* k, const double* v, const double* dO,
                          int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale, int wl,
-                         int wr, const double* slopes, const int64_t* units, int64_t n_units,
-                         double* dq, double* dk, double* dv, double* o, double* lse) {
+                         int wr, const double* slopes, const int* seqlens_k,
+                         const int64_t* units, int64_t n_units, double* dq, double* dk,
+                         double* dv, double* o, double* lse) {
   int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
   if (rc) return rc;
   for (int64_t u = 0; u < n_units; ++u)
@@ -415,7 +427,7 @@ int oracle_bwd_units_mod(const double* q, const double* k, const double* v, cons
 #pragma omp for schedule(dynamic, 4)
         for (long i = 0; i < Sq; ++i) {
           long lo, hi;
-          mod_key_range(i, Sk, wl, wr, &lo, &hi);
+          mod_key_range(i, batch_keys(seqlens_k, b, Sk), wl, wr, &lo, &hi);
           const double* qi = q + (row0 + i) * D;
           const double* gi_row = dO + (row0 + i) * D;
           double* oi = o + (row0 + i) * D;
@@ -445,7 +457,7 @@ int oracle_bwd_units_mod(const double* q, const double* k, const double* v, cons
         const double slope = head_slope(slopes, h);
         for (long i = 0; i < Sq; ++i) {
           long lo, hi;
-          mod_key_range(i, Sk, wl, wr, &lo, &hi);
+          mod_key_range(i, batch_keys(seqlens_k, b, Sk), wl, wr, &lo, &hi);
           if (j < lo || j >= hi) continue;
           const double* qi = q + (row0 + i) * D;
           const double* gi_row = dO + (row0 + i) * D;
@@ -486,7 +498,8 @@ int oracle_bwd_units_mod(const double* q, const double* k, const double* v, cons
  */
 int oracle_fwd_mod_range(const double* q, const double* k, const double* v, int B, int Hq,
                          int Hkv, int Sq, int Sk, int D, double scale, int wl, int wr,
-                         const double* slopes, int k0, int k1, double* o, double* lse) {
+                         const double* slopes, const int* seqlens_k, int k0, int k1, double* o,
+                         double* lse) {
   int rc = check_dims(B, Hq, Hkv, Sq, Sk, D);
   if (rc) return rc;
   if (k0 < 0 || k1 < k0 || k1 > Sk) return -3;
@@ -500,7 +513,7 @@ int oracle_fwd_mod_range(const double* q, const double* k, const double* v, int 
       const long b = bh / Hq, h = bh % Hq;
       const long kvh = b * Hkv + kv_head_of((int)h, Hq, Hkv);
       long lo, hi;
-      mod_key_range(i, Sk, wl, wr, &lo, &hi);
+      mod_key_range(i, batch_keys(seqlens_k, b, Sk), wl, wr, &lo, &hi);
       if (lo < k0) lo = k0;
       if (hi > k1) hi = k1;
       mod_fwd_row(q + flat * D, k + kvh * (long)Sk * D, v + kvh * (long)Sk * D, D, i, lo, hi,

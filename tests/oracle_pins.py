@@ -538,6 +538,60 @@ def pin_mod_bwd_invariants(lib):
            "mod sum_j dV_j = sum_i dO_i")
 
 
+def pin_mod_key_padding(lib):
+    """Per-batch key lengths: batch b with L_b keys gives what the same problem
+    gives with K and V cut to their first L_b rows (window and bias keep the
+    absolute indices, so the cut changes nothing else); L_b = 0 gives O = 0 and
+    LSE = -inf; a length above Sk is Sk.  The backward: gradients of the cut
+    problem on the kept keys, dK = dV = 0 past L_b, and dQ = 0 for rows that see
+    no key."""
+    rng = _rng(27)
+    B, Hq, Hkv, Sq, Sk, D = 4, 2, 1, 9, 11, 4
+    q = _rand(rng, B, Hq, Sq, D, std=1.5)
+    k = _rand(rng, B, Hkv, Sk, D, std=1.5)
+    v = _rand(rng, B, Hkv, Sk, D)
+    do = _rand(rng, B, Hq, Sq, D)
+    lens = np.array([7, 0, 11, 40], dtype=np.int32)
+    slopes = [0.4, -0.9]
+    for wl, wr in ((3, 1), (-1, -1), (-1, 0)):
+        o, lse = oracle.fwd_mod(q, k, v, 0.7, wl, wr, slopes=slopes, seqlens_k=lens, lib=lib)
+        dq, dk, dv, o2, lse2 = oracle.bwd_mod(q, k, v, do, 0.7, wl, wr, slopes=slopes,
+                                              seqlens_k=lens, lib=lib)
+        _close(o2, o, 0.0, f"padding bwd O = fwd O ({wl},{wr})")
+        for b in range(B):
+            L = min(int(lens[b]), Sk)
+            tag = f"padding b={b} L={L} window ({wl},{wr})"
+            if L == 0:
+                assert np.all(o[b] == 0.0) and np.all(np.isneginf(lse[b])), tag + ": empty"
+                assert np.all(dq[b] == 0.0) and np.all(dk[b] == 0.0) and np.all(dv[b] == 0.0)
+                continue
+            sl = (slice(b, b + 1), slice(None), slice(0, L))
+            oc, lc = oracle.fwd_mod(q[b:b + 1], k[sl], v[sl], 0.7, wl, wr, slopes=slopes, lib=lib)
+            _close(o[b:b + 1], oc, 1e-15, tag + ": O")
+            _close(lse[b:b + 1], lc, 1e-15, tag + ": LSE")
+            gq, gk, gv, _, _ = oracle.bwd_mod(q[b:b + 1], k[sl], v[sl], do[b:b + 1], 0.7, wl, wr,
+                                              slopes=slopes, lib=lib)
+            _close(dq[b:b + 1], gq, 1e-15, tag + ": dQ")
+            _close(dk[sl], gk, 1e-15, tag + ": dK")
+            _close(dv[sl], gv, 1e-15, tag + ": dV")
+            assert np.all(dk[b, :, L:] == 0.0) and np.all(dv[b, :, L:] == 0.0), tag + ": tail"
+        # the key-range form with lengths merges back to the full result
+        parts = [oracle.fwd_mod_range(q, k, v, 0.7, a, c, wl, wr, slopes=slopes,
+                                      seqlens_k=lens, lib=lib) for a, c in ((0, 4), (4, 11))]
+        om, lm = oracle.lse_merge(np.stack([p[0] for p in parts]),
+                                  np.stack([p[1] for p in parts]), lib=lib)
+        _close(om, o, 1e-12, f"padding merged O ({wl},{wr})")
+        live = np.isfinite(lse)
+        assert np.array_equal(np.isneginf(lm), ~live), f"padding merged empty rows ({wl},{wr})"
+        _close(lm[live], lse[live], 1e-12, f"padding merged LSE ({wl},{wr})")
+    rows = [0, Sq + 3, 2 * Hq * Sq - 1, 3 * Hq * Sq + 5]
+    orow, lrow = oracle.fwd_rows_mod(q, k, v, 0.7, rows, 3, 1, slopes=slopes, seqlens_k=lens,
+                                     lib=lib)
+    o, lse = oracle.fwd_mod(q, k, v, 0.7, 3, 1, slopes=slopes, seqlens_k=lens, lib=lib)
+    _close(orow, o.reshape(-1, D)[rows], 0.0, "padding rows O")
+    assert np.array_equal(lrow, lse.reshape(-1)[rows]), "padding rows LSE"
+
+
 # --------------------------------------------------------------------------- split-KV
 
 
@@ -625,7 +679,8 @@ SPLIT_PINS = [pin_split_partition, pin_split_range_special_cases, pin_merge_clos
 
 
 MOD_PINS = [pin_mod_window_zero, pin_mod_alibi_identical_keys, pin_mod_dense_brute_force,
-            pin_mod_reduces_to_plain, pin_mod_bwd_finite_differences, pin_mod_bwd_invariants]
+            pin_mod_reduces_to_plain, pin_mod_bwd_finite_differences, pin_mod_bwd_invariants,
+            pin_mod_key_padding]
 
 FWD_PINS = [pin_hand_example, pin_identical_keys, pin_causal_row0, pin_scale_zero,
             pin_single_key, pin_library_routines, pin_softmax_rows_sum_to_one, pin_key_permutation,

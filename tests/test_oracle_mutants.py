@@ -56,6 +56,10 @@ MUTANTS = {
     "mod_dq_row_term_sign": ("attn_oracle.c",
                              "const double g_w = w * (dot(gi_row, vh + j * D, D) - rterm);",
                              "const double g_w = w * (dot(gi_row, vh + j * D, D) + rterm);"),
+    "padding_length_ignored": ("attn_oracle.c", "return L < 0 ? 0 : (L > Sk ? Sk : L);",
+                               "return Sk + 0 * L;"),
+    "padding_length_inclusive": ("attn_oracle.c", "const long L = seqlens_k[b];",
+                                 "const long L = seqlens_k[b] + 1;"),
     "merge_lse_drops_max": ("attn_oracle.c", "const double row_lse = M + log(z);",
                             "const double row_lse = log(z);"),
     "merge_weights_unnormalised": ("attn_oracle.c",
