@@ -31,10 +31,11 @@ EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bw
 
 
 class ScoreMod(ctypes.Structure):
-    """fa_score_mod: a sliding window (negative sides unbounded) and optional
-    per-head relative-position bias slopes (a device pointer or None)."""
+    """fa_score_mod: a sliding window (negative sides unbounded), optional
+    per-head relative-position bias slopes and optional per-batch key counts
+    (device pointers or None)."""
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
-                ("alibi_slopes", ctypes.c_void_p)]
+                ("alibi_slopes", ctypes.c_void_p), ("seqlens_k", ctypes.c_void_p)]
 
 _LIB = None
 
@@ -89,9 +90,9 @@ def _bind(lib):
     return lib
 
 
-def _score_mod(causal, window, alibi_slopes, Hq):
+def _score_mod(causal, window, alibi_slopes, Hq, seqlens_k=None, B=None):
     """The fa_score_mod for a call, or None when the plain entry point applies."""
-    if window is None and alibi_slopes is None:
+    if window is None and alibi_slopes is None and seqlens_k is None:
         return None
     wl, wr = (-1, 0 if causal else -1) if window is None else window
     if causal and window is not None:
@@ -102,7 +103,13 @@ def _score_mod(causal, window, alibi_slopes, Hq):
                 or alibi_slopes.numel() != Hq or not alibi_slopes.is_contiguous()):
             raise TypeError("alibi_slopes must be a contiguous fp32 CUDA tensor of Hq slopes")
         ptr = alibi_slopes.data_ptr()
-    return ScoreMod(int(wl), int(wr), ptr)
+    lens = None
+    if seqlens_k is not None:
+        if (not seqlens_k.is_cuda or seqlens_k.dtype != torch.int32
+                or seqlens_k.numel() != B or not seqlens_k.is_contiguous()):
+            raise TypeError("seqlens_k must be a contiguous int32 CUDA tensor of B key counts")
+        lens = seqlens_k.data_ptr()
+    return ScoreMod(int(wl), int(wr), ptr, lens)
 
 
 def lib():
@@ -144,11 +151,13 @@ def _ptr(t):
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: float | None = None, out: torch.Tensor | None = None,
         lse: torch.Tensor | None = None, stream=None, window=None, alibi_slopes=None,
-        n_splits: int | None = None, split_workspace: torch.Tensor | None = None):
+        n_splits: int | None = None, split_workspace: torch.Tensor | None = None,
+        seqlens_k: torch.Tensor | None = None):
     """Forward attention. q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA.
 
-    ``window=(left, right)`` and ``alibi_slopes`` (fp32 [Hq]) select the score
-    modification of fa_fwd_mod (include/fa.h).  ``n_splits`` (0: automatic)
+    ``window=(left, right)``, ``alibi_slopes`` (fp32 [Hq]) and ``seqlens_k``
+    (int32 [B] key counts: the key padding mask) select the score modification
+    of fa_fwd_mod (include/fa.h); a row that sees no key gets O = 0, LSE = -inf.  ``n_splits`` (0: automatic)
     runs the split-KV form fa_fwd_split; its workspace is ``split_workspace``
     (uint8 CUDA) or allocated here.
     Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] fp32, natural log).
@@ -163,10 +172,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
-    mod = _score_mod(causal, window, alibi_slopes, Hq)
+    mod = _score_mod(causal, window, alibi_slopes, Hq, seqlens_k, B)
     if n_splits is not None:
         if mod is None and causal:
-            mod = ScoreMod(-1, 0, None)
+            mod = ScoreMod(-1, 0, None, None)
         ws_bytes = fwd_split_workspace_bytes(B, Hq, Sq, Sk, D, n_splits)
         if split_workspace is None:
             split_workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
@@ -229,9 +238,11 @@ def bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, deterministic=False) -> int:
 
 def bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
         deterministic: bool = False, workspace: torch.Tensor | None = None,
-        dq=None, dk=None, dv=None, stream=None, window=None, alibi_slopes=None):
+        dq=None, dk=None, dv=None, stream=None, window=None, alibi_slopes=None,
+        seqlens_k=None):
     """Backward attention. Returns (dq, dk, dv) bf16, same shapes as q, k, v.
-    ``window`` / ``alibi_slopes`` as in fwd (must match the forward call)."""
+    ``window`` / ``alibi_slopes`` / ``seqlens_k`` as in fwd (must match the
+    forward call)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _check(t, n)
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
@@ -246,7 +257,7 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    mod = _score_mod(causal, window, alibi_slopes, Hq)
+    mod = _score_mod(causal, window, alibi_slopes, Hq, seqlens_k, B)
     if mod is None:
         rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                           _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
@@ -316,29 +327,32 @@ class _Attention(torch.autograd.Function):
     """fwd in forward (saving O and LSE), bwd in backward; nothing else runs."""
 
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale, window, alibi_slopes, deterministic):
+    def forward(ctx, q, k, v, causal, scale, window, alibi_slopes, deterministic, seqlens_k):
         o, lse = fwd(q, k, v, causal=causal, scale=scale, window=window,
-                     alibi_slopes=alibi_slopes)
+                     alibi_slopes=alibi_slopes, seqlens_k=seqlens_k)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.args = (causal, scale, window, alibi_slopes, deterministic)
+        ctx.args = (causal, scale, window, alibi_slopes, deterministic, seqlens_k)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        causal, scale, window, alibi_slopes, deterministic = ctx.args
+        causal, scale, window, alibi_slopes, deterministic, seqlens_k = ctx.args
         dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, causal=causal, scale=scale,
-                         deterministic=deterministic, window=window, alibi_slopes=alibi_slopes)
-        return dq, dk, dv, None, None, None, None, None
+                         deterministic=deterministic, window=window, alibi_slopes=alibi_slopes,
+                         seqlens_k=seqlens_k)
+        return dq, dk, dv, None, None, None, None, None, None
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
               scale: float | None = None, window=None, alibi_slopes=None,
-              deterministic: bool = False) -> torch.Tensor:
+              deterministic: bool = False, seqlens_k=None) -> torch.Tensor:
     """Exact attention as a differentiable op: O = softmax(scale q k^T + mods) v.
 
-    q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA; ``causal``, ``window`` and
-    ``alibi_slopes`` as in fwd; ``deterministic`` selects the backward mode.
-    O.backward() runs fa_bwd (the slopes get no gradient).  Returns O bf16.
+    q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] bf16 CUDA; ``causal``, ``window``,
+    ``alibi_slopes`` and ``seqlens_k`` as in fwd; ``deterministic`` selects the
+    backward mode.  O.backward() runs fa_bwd (the slopes get no gradient).
+    Returns O bf16.
     """
-    return _Attention.apply(q, k, v, causal, scale, window, alibi_slopes, deterministic)
+    return _Attention.apply(q, k, v, causal, scale, window, alibi_slopes, deterministic,
+                            seqlens_k)

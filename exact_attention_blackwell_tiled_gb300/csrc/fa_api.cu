@@ -57,24 +57,27 @@ int check_shape(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
   return FA_OK;
 }
 
-// A call's visibility window and relative-position bias (fa_score_mod).
+// A call's visibility window, relative-position bias and key lengths
+// (fa_score_mod).
 struct ModArgs {
   int wl, wr;
   const float* alibi;
+  const int* seqlens_k;
 };
 
-ModArgs plain_mod(int causal) { return ModArgs{-1, causal ? 0 : -1, nullptr}; }
+ModArgs plain_mod(int causal) { return ModArgs{-1, causal ? 0 : -1, nullptr, nullptr}; }
 
 ModArgs read_mod(const fa_score_mod* m) {
   if (!m) return plain_mod(0);
   return ModArgs{m->window_left < 0 ? -1 : m->window_left,
-                 m->window_right < 0 ? -1 : m->window_right, m->alibi_slopes};
+                 m->window_right < 0 ? -1 : m->window_right, m->alibi_slopes, m->seqlens_k};
 }
 
-// Every query row must see a key: the last row sees keys from Sq - 1 - wl on.
-int check_mod(const ModArgs& m, int Sq, int Sk) {
-  if (m.wl >= 0 && (long long)m.wl < (long long)Sq - Sk) return FA_ERR_INVALID_ARG;
+// The device arrays a modification reads are 4-byte aligned.  (A row that sees
+// no key is allowed: O = 0, LSE = -inf.)
+int check_mod(const ModArgs& m) {
   if (m.alibi && (reinterpret_cast<uintptr_t>(m.alibi) & 3)) return FA_ERR_MISALIGNED;
+  if (m.seqlens_k && (reinterpret_cast<uintptr_t>(m.seqlens_k) & 3)) return FA_ERR_MISALIGNED;
   return FA_OK;
 }
 
@@ -198,7 +201,7 @@ int fwd_setup(const void* q, const void* k, const void* v, void* o, float* lse, 
   *nothing = false;
   int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc) return rc;
-  if ((rc = check_mod(m, Sq, Sk))) return rc;
+  if ((rc = check_mod(m))) return rc;
   if (Sq == 0) {  // nothing to read or write; q, o, lse may be null
     *nothing = true;
     return FA_OK;
@@ -222,6 +225,7 @@ int fwd_setup(const void* q, const void* k, const void* v, void* o, float* lse, 
   a->wl = m.wl;
   a->wr = m.wr;
   a->alibi = m.alibi;
+  a->seqlens_k = m.seqlens_k;
   a->scale_log2 = scale * 1.4426950408889634f;
   a->n_qtiles = (Sq + kTile - 1) / kTile;
   a->n_pairs = (a->n_qtiles + 1) / 2;
@@ -398,7 +402,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   t_launches = 0;
   int rc = check_shape(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc) return rc;
-  if ((rc = check_mod(m, Sq, Sk))) return rc;
+  if ((rc = check_mod(m))) return rc;
   // With Sq == 0 the query-side tensors are empty and may be null; dk and dv
   // are still written (as zeros).
   const bool has_q = Sq > 0;
@@ -456,6 +460,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.wl = m.wl;
   a.wr = m.wr;
   a.alibi = has_q ? m.alibi : nullptr;
+  a.seqlens_k = has_q ? m.seqlens_k : nullptr;  // with no queries dK = dV = 0 anyway
   // longest-first snake when the streamed queries and output gradients
   // (q, dO) fit comfortably in L2
   a.snake = (a.causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;

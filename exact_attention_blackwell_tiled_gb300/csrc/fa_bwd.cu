@@ -30,7 +30,8 @@
 //                      the group's first contributor stores.  At the end of the
 //                      unit dK_j * scale and dV_j are written as bf16.
 //   3. bwd_dq_convert  dQ = scale * accumulator -> bf16 (deterministic mode: the
-//                      sum of the groups' accumulators in fixed order).
+//                      sum of the groups' accumulators in fixed order, each
+//                      group whose semaphore shows a writer).
 //
 // bwd_main warp roles, with n = 8 softmax warps (plain D = 128 kernel: 512
 // threads, 128 registers) or n = 16 (score-modified and D = 64 kernels: 768
@@ -228,24 +229,41 @@ __device__ __forceinline__ int win_right(const BwdArgs& a) {
   return kMod ? a.wr : (a.causal ? 0 : -1);
 }
 
-// 64-row query blocks [lo, hi) with a query that sees a key of kv tile j: the
-// queries from (first key - wr) to (last key + wl)
+// Keys of batch b that exist: seqlens_k[b] clamped to [0, Sk] (the key padding
+// mask); all Sk without lengths, and always in the plain kernel.
 template <bool kMod>
-__device__ __forceinline__ void bwd_qblk_range(const BwdArgs& a, int j, int& lo, int& hi) {
+__device__ __forceinline__ int bwd_kv_len(const BwdArgs& a, int b) {
+  if (!kMod || !a.seqlens_k) return a.Sk;
+  const int n = __ldg(a.seqlens_k + b);
+  return n < 0 ? 0 : (n < a.Sk ? n : a.Sk);
+}
+
+// 64-row query blocks [lo, hi) with a query that sees a key of kv tile j (of a
+// batch with kv_len keys): the queries from (first key - wr) to (last key +
+// wl); empty when the tile holds no key of the batch
+template <bool kMod>
+__device__ __forceinline__ void bwd_qblk_range(const BwdArgs& a, int j, int kv_len, int& lo,
+                                               int& hi) {
   const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
-  const int k0 = j * kTile, k1 = min(a.Sk, k0 + kTile) - 1;
+  const int k0 = j * kTile;
+  if (k0 >= kv_len) {
+    lo = hi = 0;
+    return;
+  }
+  const int k1 = min(kv_len, k0 + kTile) - 1;
   const int q_lo = wr >= 0 ? max(0, k0 - wr) : 0;
   const int q_hi = wl >= 0 ? min(a.Sq - 1, k1 + wl) : a.Sq - 1;
   lo = q_lo / kQB;
   hi = q_hi >= q_lo ? q_hi / kQB + 1 : lo;
 }
 
-// The kv tiles [first, last] that add into 64-row query block iq under the
-// window (wl, wr): those whose query-block range (bwd_qblk_range) holds iq.
-__device__ __forceinline__ void qblk_contributors(const BwdArgs& a, int wl, int wr, int iq,
-                                                  int& first, int& last) {
-  first = wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
-  last = wr >= 0 ? min(a.n_ktiles - 1, (iq * kQB + kQB - 1 + wr) / kTile) : a.n_ktiles - 1;
+// The first kv tile that adds into 64-row query block iq: the kv tiles that do
+// (those whose bwd_qblk_range holds iq) are a contiguous run, since both ends
+// of that range grow with j, and the run starts at the first tile whose last
+// key reaches the block's first query - wl.  (The bound can overshoot only when
+// no tile adds at all, which a caller that adds never meets.)
+__device__ __forceinline__ int qblk_first_contributor(int wl, int iq) {
+  return wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
 }
 
 // The first kv tile >= first that belongs to deterministic group g.
@@ -348,6 +366,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16
 // Iterations (q head of the group x query block) of kv tile j.
 struct BwdUnit {
   int bhk, j, b, hk, lo, n_blk, n_it;
+  int kv_len;  // keys of batch b
 };
 
 // The r-th unit this CTA processes (-1 when it has no more).  Units are either
@@ -376,8 +395,9 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
   }
   w.b = w.bhk / a.Hkv;
   w.hk = w.bhk - w.b * a.Hkv;
+  w.kv_len = bwd_kv_len<kMod>(a, w.b);
   int hi;
-  bwd_qblk_range<kMod>(a, w.j, w.lo, hi);
+  bwd_qblk_range<kMod>(a, w.j, w.kv_len, w.lo, hi);
   w.n_blk = hi - w.lo;
   w.n_it = group * w.n_blk;
   return w;
@@ -656,7 +676,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
       const BwdUnit w = bwd_unit<kMod>(a, u, group);
       const int kv = w.j * kTile + r;
-      const bool row_dead = kv >= a.Sk;
+      const bool row_dead = kv >= w.kv_len;
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
@@ -799,8 +819,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           // deterministic mode: kv tile j adds into accumulator g = j % G after
           // the tiles of its group before it (from the block's first
           // contributor on); the first of them stores instead of adding
-          int first, last;
-          qblk_contributors(a, win_left<kMod>(a), win_right<kMod>(a), iq, first, last);
+          const int first = qblk_first_contributor(win_left<kMod>(a), iq);
           const int g = w.j % a.dq_groups;
           const int turn = (w.j - group_first(first, g, a.dq_groups)) / a.dq_groups;
           float* dst = a.dq_acc + (size_t)g * a.dq_group_stride +
@@ -938,13 +957,13 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
     float4 x0 = reinterpret_cast<const float4*>(base)[0];
     float4 x1 = reinterpret_cast<const float4*>(base)[1];
     if (a.deterministic) {
-      // the groups' accumulators in fixed order; a group with no contributing
-      // kv tile for this query block was never written
-      int first, last;
-      qblk_contributors(a, a.wl, a.wr, (int)(i / kQB), first, last);
-      if (group_first(first, 0, a.dq_groups) > last) x0 = x1 = make_float4(0.f, 0.f, 0.f, 0.f);
+      // the groups' accumulators in fixed order; a group that no kv tile
+      // wrote for this query block (its semaphore, the count of warps that
+      // added, is 0) holds stale memory and is skipped
+      const int* sem = a.sem + (size_t)bh * a.n_qblk + i / kQB;
+      if (__ldg(sem) == 0) x0 = x1 = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int g = 1; g < a.dq_groups; ++g) {
-        if (group_first(first, g, a.dq_groups) > last) continue;
+        if (__ldg(sem + (size_t)g * a.sem_group_stride) == 0) continue;
         const float4* src = reinterpret_cast<const float4*>(base + (size_t)g * a.dq_group_stride);
         const float4 y0 = src[0], y1 = src[1];
         x0.x += y0.x, x0.y += y0.y, x0.z += y0.z, x0.w += y0.w;
@@ -991,8 +1010,10 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   //    in-order semaphore chain relies on)
   {
     const int grid = a.n_units < sms ? a.n_units : sms;
-    // a window other than none / causal, or a bias, selects the general kernel
-    const bool mod = a.alibi || !(a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal)));
+    // a window other than none / causal, a bias or key lengths select the
+    // general kernel
+    const bool mod =
+        a.alibi || a.seqlens_k || !(a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal)));
     const auto kernel = mod ? bwd_main<D, true> : bwd_main<D, false>;
     const int threads =
         (mod || D == 64) ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;

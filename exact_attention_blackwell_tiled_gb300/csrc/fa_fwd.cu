@@ -121,24 +121,33 @@ __device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, in
   pair = a.causal ? ((r & 1) ? (r >> 1) : (np - 1 - (r >> 1))) : r;
 }
 
-// kv tiles [lo, hi) that query tile qt sees under the window (wl, wr) (empty
-// when the tile lies past Sq)
-__device__ __forceinline__ void tile_kv_range(const FwdArgs& a, int wl, int wr, int qt, int& lo,
-                                              int& hi) {
+// Keys of batch b that exist: seqlens_k[b] clamped to [0, Sk] (the key padding
+// mask); all Sk without lengths, and always in the plain kernel.
+template <bool kWin>
+__device__ __forceinline__ int batch_kv_len(const FwdArgs& a, int b) {
+  if (!kWin || !a.seqlens_k) return a.Sk;
+  const int n = __ldg(a.seqlens_k + b);
+  return n < 0 ? 0 : (n < a.Sk ? n : a.Sk);
+}
+
+// kv tiles [lo, hi) that query tile qt sees under the window (wl, wr) among the
+// first kv_len keys (empty when the tile lies past Sq or sees no key)
+__device__ __forceinline__ void tile_kv_range(const FwdArgs& a, int wl, int wr, int kv_len, int qt,
+                                              int& lo, int& hi) {
   lo = hi = 0;
   if (qt * kTile >= a.Sq) return;
   const int last = min(a.Sq, (qt + 1) * kTile) - 1;  // last query row of the tile
   const int lo_key = wl >= 0 ? max(0, qt * kTile - wl) : 0;
-  const int hi_key = wr >= 0 ? min(a.Sk, last + wr + 1) : a.Sk;
+  const int hi_key = wr >= 0 ? min(kv_len, last + wr + 1) : kv_len;
   lo = lo_key / kTile;
   hi = max(lo, (hi_key + kTile - 1) / kTile);
 }
 
 // A tile's range cut to the kv tiles of `split` (kSplit); may become empty.
 template <bool kSplit>
-__device__ __forceinline__ void split_kv_range(const FwdArgs& a, int wl, int wr, int qt, int split,
-                                               int& lo, int& hi) {
-  tile_kv_range(a, wl, wr, qt, lo, hi);
+__device__ __forceinline__ void split_kv_range(const FwdArgs& a, int wl, int wr, int kv_len, int qt,
+                                               int split, int& lo, int& hi) {
+  tile_kv_range(a, wl, wr, kv_len, qt, lo, hi);
   if (kSplit) {
     const int s0 = split * a.split_tiles;
     lo = max(lo, s0);
@@ -150,10 +159,10 @@ __device__ __forceinline__ void split_kv_range(const FwdArgs& a, int wl, int wr,
 // and their union [jlo, jlo + nmax).  An empty tile gets lo = hi = jlo; both
 // empty: nmax = 0 and the unit is skipped.
 template <bool kSplit>
-__device__ __forceinline__ void pair_kv_span(const FwdArgs& a, int wl, int wr, int pair, int split,
-                                             int lo[2], int hi[2], int& jlo, int& nmax) {
-  split_kv_range<kSplit>(a, wl, wr, 2 * pair, split, lo[0], hi[0]);
-  split_kv_range<kSplit>(a, wl, wr, 2 * pair + 1, split, lo[1], hi[1]);
+__device__ __forceinline__ void pair_kv_span(const FwdArgs& a, int wl, int wr, int kv_len, int pair,
+                                             int split, int lo[2], int hi[2], int& jlo, int& nmax) {
+  split_kv_range<kSplit>(a, wl, wr, kv_len, 2 * pair, split, lo[0], hi[0]);
+  split_kv_range<kSplit>(a, wl, wr, kv_len, 2 * pair + 1, split, lo[1], hi[1]);
   const bool e0 = hi[0] <= lo[0], e1 = hi[1] <= lo[1];
   if (e0 && e1) {
     jlo = lo[0];
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(320, 1)
         const int b = bh / a.Hq, h = bh - b * a.Hq;
         const int bhk = b * a.Hkv + h / group;
         int lo[2], hi[2], jlo, nmax;
-        pair_kv_span<kSplit>(a, wl, wr, pair, split, lo, hi, jlo, nmax);
+        pair_kv_span<kSplit>(a, wl, wr, batch_kv_len<kWin>(a, b), pair, split, lo, hi, jlo, nmax);
         if (nmax == 0) continue;
         const uint32_t qs = q_it % L::kQStages;
         if (!mbar_wait(bar(L::kBarQEmpty + qs), ((q_it / L::kQStages) & 1) ^ 1, abort_flag)) {
@@ -307,7 +316,8 @@ __global__ void __launch_bounds__(320, 1)
         // kv tile j sits at position p = j - jlo of the pair's range; tile t
         // computes S for positions [plo[t], phi[t]) and O one position behind
         int plo[2], phi[2], jlo, nmax;
-        pair_kv_span<kSplit>(a, wl, wr, pair, split, plo, phi, jlo, nmax);
+        pair_kv_span<kSplit>(a, wl, wr, batch_kv_len<kWin>(a, bh / a.Hq), pair, split, plo, phi,
+                             jlo, nmax);
         if (nmax == 0) continue;
         for (int t = 0; t < 2; ++t) {
           plo[t] -= jlo;
@@ -406,17 +416,26 @@ __global__ void __launch_bounds__(320, 1)
       int bh, pair, split;
       unit_coords(a, u, bh, pair, split);
       const int qt = 2 * pair + t;
+      const int kv_len = batch_kv_len<kWin>(a, bh / a.Hq);
       int jlo, jhi;
-      split_kv_range<kSplit>(a, wl, wr, qt, split, jlo, jhi);
+      split_kv_range<kSplit>(a, wl, wr, kv_len, qt, split, jlo, jhi);
       const int q_row = qt * kTile + r;
       const size_t part_row = ((size_t)split * a.B * a.Hq + bh) * a.Sq + q_row;
       if (jhi == jlo) {
-        // no key of this split reaches the tile: an empty part
+        // no key (of this split) reaches the tile: an empty part, or with a
+        // window or padding the whole tile sees no key: O = 0, LSE = -inf
         if (kSplit && q_row < a.Sq) a.lse_part[part_row] = -INFINITY;
+        if (!kSplit && kWin && q_row < a.Sq) {
+          uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                                 ((size_t)bh * a.Sq + q_row) * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+          a.lse[(size_t)bh * a.Sq + q_row] = -INFINITY;
+        }
         continue;
       }
       // keys [lo_row, lim) are visible to this row
-      const int lim = wr >= 0 ? min(a.Sk, q_row + wr + 1) : a.Sk;
+      const int lim = wr >= 0 ? min(kv_len, q_row + wr + 1) : kv_len;
       const int lo_row = wl >= 0 ? max(0, q_row - wl) : 0;
       auto hidden = [&](int key) { return key >= lim || (kWin && key < lo_row); };
       // relative-position bias in log2 units: slope * log2(e) per key offset,
@@ -592,8 +611,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool row_ok = q_row < a.Sq;
       if (kSplit) {
         // fp32 part: O / l and the part's LSE; a row with no visible key in
-        // this split (l = 0) is an empty part, O = 0 and LSE = -inf
-        const bool empty = !(l_run > 0.f);
+        // this split (its running max still -inf) is an empty part, O = 0 and
+        // LSE = -inf.  (l alone does not show it: the polynomial 2^x gives a
+        // tiny positive value, not 0, for the -inf of a hidden key.)
+        const bool empty = m_run == -INFINITY || !(l_run > 0.f);
         const float inv = empty ? 0.f : 1.0f / l_run;
         // rows grp_row0 .. +3 of the lane group trade 16-byte pieces as in the
         // bf16 epilogue below, in two rounds of four pieces
@@ -635,7 +656,11 @@ __global__ void __launch_bounds__(320, 1)
               empty ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994531f;
         continue;
       }
-      const float inv_l = 1.0f / l_run;
+      // a row that sees no key (a window or padding) keeps the running max at
+      // -inf: O = 0, LSE = -inf
+      const bool no_key = kWin && (m_run == -INFINITY || !(l_run > 0.f));
+      const float inv_l = no_key ? 0.f : 1.0f / l_run;
+      const float row_lse = no_key ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994531f;
       if constexpr (D == 128) {
         // Each thread holds one row; so that a store instruction writes whole
         // 64-byte row pieces instead of 16 bytes of 32 rows, the four lanes of
@@ -671,8 +696,7 @@ __global__ void __launch_bounds__(320, 1)
                   make_uint4(w[4 * m], w[4 * m + 1], w[4 * m + 2], w[4 * m + 3]);
           }
         }
-        if (row_ok)
-          a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        if (row_ok) a.lse[(size_t)bh * a.Sq + q_row] = row_lse;
       } else {
         // D = 64: each thread stores its own row, and O is released after the
         // stores (both measured faster here than the D = 128 form, whose
@@ -695,8 +719,7 @@ __global__ void __launch_bounds__(320, 1)
               dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
-        if (row_ok)
-          a.lse[(size_t)bh * a.Sq + q_row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        if (row_ok) a.lse[(size_t)bh * a.Sq + q_row] = row_lse;
         tc_fence_before();
         mbar_arrive(bar(L::kBarOFree + t));
       }
@@ -761,9 +784,10 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     grid = a.n_units < sms ? a.n_units : sms;
   }
   record_timing(false, stream);
-  // a window other than none / causal, or a bias, selects the general kernel
+  // a window other than none / causal, a bias or key lengths select the general
+  // kernel
   const bool plain_window = a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal));
-  const int mode = a.alibi ? 2 : (plain_window ? 0 : 1);
+  const int mode = a.alibi ? 2 : ((plain_window && !a.seqlens_k) ? 0 : 1);
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs);
   const KernelFn kernels[2][3] = {{fwd_kernel<D, 0, false>, fwd_kernel<D, 1, false>,
                                    fwd_kernel<D, 2, false>},

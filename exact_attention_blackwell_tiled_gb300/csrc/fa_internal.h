@@ -39,6 +39,9 @@ struct FwdArgs {
   // (wr < 0 || j <= i + wr); causal is wl = -1, wr = 0
   int wl, wr;
   const float* alibi;  // [Hq] slopes of the relative-position bias, or null
+  // [B] keys per batch (key padding mask: keys j >= seqlens_k[b] are hidden;
+  // clamped to [0, Sk]), or null
+  const int* seqlens_k;
   float scale_log2;  // scale * log2(e)
   int n_qtiles;
   int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
@@ -87,9 +90,10 @@ struct BwdArgs {
   int B, Hq, Hkv, Sq, Sk, D;
   int Sq_pad;
   int causal;
-  // visibility window and relative-position bias, as in FwdArgs
+  // visibility window, relative-position bias and key lengths, as in FwdArgs
   int wl, wr;
   const float* alibi;
+  const int* seqlens_k;
   int deterministic;
   float scale;
   float scale_log2;

@@ -71,24 +71,30 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Hkv, int Sq, int Sk, int D, int causal, float scale, fa_stream_t stream);
 
 /*
- * Score modification: a sliding-window mask and a linear relative-position bias
- * (FlashAttention-4 pages, "CuTe-DSL Implementation and Rapid JIT Compilation":
- * the FlexAttention integration's score modifications, relative position biases
- * and masks, which the pages name without defining).  Key kv_idx is visible to
- * query q_idx iff
+ * Score modification: a sliding-window mask, a key padding mask and a linear
+ * relative-position bias (FlashAttention-4 pages, "CuTe-DSL Implementation and
+ * Rapid JIT Compilation": the FlexAttention integration's score modifications,
+ * relative position biases and custom masks, which the pages name without
+ * defining).  Key kv_idx of batch b is visible to query q_idx iff
  *   (window_left  < 0 || kv_idx >= q_idx - window_left) &&
- *   (window_right < 0 || kv_idx <= q_idx + window_right),
- * so {-1, 0} is fa_fwd's causal mask and {-1, -1} no mask.  Every query row
- * must see a key: window_left < 0 or window_left >= Sq - Sk (else
- * FA_ERR_INVALID_ARG).  alibi_slopes is null or a device array of Hq fp32
- * slopes (4-byte aligned, else FA_ERR_MISALIGNED, left unread when Sq == 0);
- * the score of (q_idx, kv_idx) in query head h becomes
- * scale * q.k + alibi_slopes[h] * (kv_idx - q_idx).
+ *   (window_right < 0 || kv_idx <= q_idx + window_right) &&
+ *   (seqlens_k == NULL || kv_idx < seqlens_k[b]),
+ * so {-1, 0, NULL} is fa_fwd's causal mask and {-1, -1, NULL} no mask.
+ * seqlens_k is null or a device array of B int32 key counts (4-byte aligned,
+ * else FA_ERR_MISALIGNED; each clamped to [0, Sk]).  The keys past a batch's
+ * count are still read from k and v (with weight 0), so they must hold finite
+ * values.  A query row that sees no key gets O = 0 and LSE = -inf, and the
+ * backward gives it dQ = 0; keys no row sees get dK = dV = 0.
+ * alibi_slopes is null or a device array of Hq fp32 slopes (4-byte aligned,
+ * else FA_ERR_MISALIGNED); the score of (q_idx, kv_idx) in query head h becomes
+ * scale * q.k + alibi_slopes[h] * (kv_idx - q_idx).  Neither array is read when
+ * Sq == 0.
  */
 typedef struct {
   int window_left;
   int window_right;
   const float* alibi_slopes;
+  const int* seqlens_k;
 } fa_score_mod;
 
 /*

@@ -108,17 +108,26 @@ def test_row_count_limit(L):
 
 
 def test_score_mod_validation(L):
-    mod = fa.ScoreMod(64, -1, None)  # the last query row would see no key
-    assert L.fa_fwd_mod(P16, P16, P16, P16, P16, 1, 1, 1, 256, 128, 64, ctypes.byref(mod), 1.0,
-                        None) == 1
-    assert L.fa_bwd_mod(P16, P16, P16, P16, P16, P16, P16, P16, P16, 1, 1, 1, 256, 128, 64,
-                        ctypes.byref(mod), 1.0, P16, 1 << 30, 0, None) == 1
     bad = fa.ScoreMod(-1, 0, 16 * 1024 + 2)  # slopes must be 4-byte aligned
     assert L.fa_fwd_mod(P16, P16, P16, P16, P16, 1, 1, 1, 128, 128, 64, ctypes.byref(bad), 1.0,
                         None) == 3
-    ok = fa.ScoreMod(128, -1, None)  # window_left = Sq - Sk is the smallest allowed
+    bad = fa.ScoreMod(-1, -1, None, 16 * 1024 + 1)  # key counts must be 4-byte aligned
+    assert L.fa_fwd_mod(P16, P16, P16, P16, P16, 2, 1, 1, 128, 128, 64, ctypes.byref(bad), 1.0,
+                        None) == 3
+    assert L.fa_bwd_mod(P16, P16, P16, P16, P16, P16, P16, P16, P16, 2, 1, 1, 128, 128, 64,
+                        ctypes.byref(bad), 1.0, P16, 1 << 30, 0, None) == 3
+    # a window that leaves the last rows with no key is accepted (they get O = 0
+    # and LSE = -inf); with Sq = 0 the call reads and writes nothing
+    ok = fa.ScoreMod(64, -1, None, None)
     assert L.fa_fwd_mod(None, P16, P16, None, None, 1, 1, 1, 0, 128, 64, ctypes.byref(ok), 1.0,
                         None) == 0
+
+
+def test_score_mod_layout():
+    """The ctypes mirror of fa_score_mod matches the C layout: two ints, then the
+    two device pointers."""
+    assert ctypes.sizeof(fa.ScoreMod) == 24
+    assert fa.ScoreMod.alibi_slopes.offset == 8 and fa.ScoreMod.seqlens_k.offset == 16
 
 
 def test_split_plan(L):
@@ -154,8 +163,8 @@ def test_split_validation(L):
     assert split(q=None) == 1
     assert split(q=P17) == 3
     assert split(Sq=0, q=None) == 0  # nothing to do
-    bad = fa.ScoreMod(10, -1, None)  # leaves the last rows without a key
-    assert split(Sq=2048, mod=ctypes.byref(bad)) == 1
+    bad = fa.ScoreMod(-1, -1, None, 16 * 1024 + 2)  # misaligned key counts
+    assert split(mod=ctypes.byref(bad)) == 3
 
 
 def test_merge_validation(L):
