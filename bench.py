@@ -467,29 +467,38 @@ def visible_pairs(Sq: int, Sk: int, wl: int, wr: int) -> int:
     return int(np.maximum(0, hi - lo + 1).sum())
 
 
-# B, H, S, D, window_left, window_right, bias
+# padded batch: keys per batch element as fractions of S, repeated over B
+PAD_FRACS = (1.0, 0.75, 0.5, 0.25)
+
+# B, H, S, D, window_left, window_right, bias, padded
 MOD_SWEEP = [
-    (1, 16, 16384, 128, -1, 0, False),     # causal (the plain kernels)
-    (1, 16, 16384, 128, -1, 0, True),      # causal with the relative-position bias
-    (1, 16, 16384, 128, 1023, 0, False),   # causal local window of 1024 keys
-    (1, 16, 16384, 128, 4095, 0, False),   # causal local window of 4096 keys
-    (1, 16, 16384, 128, 512, 512, True),   # two-sided window of 1025 keys with the bias
-    (4, 16, 2048, 128, 255, 0, False),     # the train shape with a 256-key local window
+    (1, 16, 16384, 128, -1, 0, False, False),     # causal (the plain kernels)
+    (1, 16, 16384, 128, -1, 0, True, False),      # causal with the relative-position bias
+    (1, 16, 16384, 128, 1023, 0, False, False),   # causal local window of 1024 keys
+    (1, 16, 16384, 128, 4095, 0, False, False),   # causal local window of 4096 keys
+    (1, 16, 16384, 128, 512, 512, True, False),   # two-sided window of 1025 keys with the bias
+    (4, 16, 2048, 128, 255, 0, False, False),     # the train shape with a 256-key local window
+    (8, 16, 4096, 128, -1, -1, False, True),      # padded batch, keys S, 3S/4, S/2, S/4
+    (8, 16, 4096, 128, -1, 0, False, True),       # the same, causal
 ]
 
 
 def mod_sweep(fa, dev, peak, iters=10):
-    """Forward and backward-main TFLOP/s with a sliding window and / or the
-    relative-position bias; FLOPs counted over the visible (query, key) pairs."""
+    """Forward and backward-main TFLOP/s with a sliding window, the
+    relative-position bias and / or the key padding mask; FLOPs counted over the
+    visible (query, key) pairs."""
     import torch
     out = []
-    for B, H, S, D, wl, wr, bias in MOD_SWEEP:
+    for B, H, S, D, wl, wr, bias, padded in MOD_SWEEP:
         gen = torch.Generator(device=dev).manual_seed(9)
         q, k, v, do = (torch.randn(B, H, S, D, device=dev, generator=gen).to(torch.bfloat16)
                        for _ in range(4))
         slopes = (torch.tensor([0.5 ** (1 + h % 8) for h in range(H)], device=dev)
                   if bias else None)
-        kw = dict(window=(wl, wr), alibi_slopes=slopes)
+        counts = [int(S * PAD_FRACS[b % len(PAD_FRACS)]) for b in range(B)] if padded else None
+        kw = dict(window=(wl, wr), alibi_slopes=slopes,
+                  seqlens_k=None if counts is None else torch.tensor(counts, dtype=torch.int32,
+                                                                      device=dev))
         ws = torch.empty(fa.bwd_workspace_bytes(B, H, H, S, S, D), dtype=torch.uint8, device=dev)
         o, lse = fa.fwd(q, k, v, **kw)
         grads = [torch.empty_like(q) for _ in range(3)]
@@ -516,10 +525,12 @@ def mod_sweep(fa, dev, peak, iters=10):
             torch.cuda.synchronize(dev)
             ms[which] = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
         assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
-        f_fwd = 4.0 * B * H * D * visible_pairs(S, S, wl, wr)
+        f_fwd = 4.0 * H * D * sum(visible_pairs(S, S if counts is None else counts[b], wl, wr)
+                                  for b in range(B))
         tf_f = f_fwd / (ms["fwd"] * 1e-3) / 1e12
         tf_b = 2.5 * f_fwd / (ms["bwd"] * 1e-3) / 1e12
         out.append({"B": B, "H": H, "S": S, "D": D, "window": [wl, wr], "bias": bias,
+                    "key_counts": counts,
                     "fwd_ms": round(ms["fwd"], 4), "fwd_tflops": round(tf_f, 1),
                     "fwd_frac": round(tf_f / peak, 4), "bwd_main_ms": round(ms["bwd"], 4),
                     "bwd_main_tflops": round(tf_b, 1), "bwd_main_frac": round(tf_b / peak, 4)})

@@ -18,12 +18,18 @@ def _built():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("mode", ["causal", "window_bias"])
+@pytest.mark.parametrize("mode", ["causal", "window_bias", "padded"])
 def test_attention_autograd(mode):
-    w = synth.Workload("autograd", 1, 4, 2, 300, 300, 128, mode == "causal", 40, with_do=True)
+    w = synth.Workload("autograd", 2, 4, 2, 300, 300, 128, mode == "causal", 40, with_do=True)
     q, k, v, do = synth.make_inputs(w, with_do=True)
-    kw = dict(causal=True) if mode == "causal" else dict(
-        window=(80, 20), alibi_slopes=torch.tensor([0.3, -0.2, 0.1, 0.5], device="cuda"))
+    lens = torch.tensor([170, 300], dtype=torch.int32)
+    if mode == "causal":
+        kw = dict(causal=True)
+    elif mode == "window_bias":
+        kw = dict(window=(80, 20),
+                  alibi_slopes=torch.tensor([0.3, -0.2, 0.1, 0.5], device="cuda"))
+    else:
+        kw = dict(window=(-1, 0), seqlens_k=lens.cuda())
     qd, kd, vd = (t.cuda().requires_grad_() for t in (q, k, v))
     o = fa.attention(qd, kd, vd, deterministic=True, **kw)
     o.backward(do.cuda())
@@ -37,6 +43,9 @@ def test_attention_autograd(mode):
     # and the oracle's gradients
     if mode == "causal":
         dq_r, dk_r, dv_r, _, _ = oracle.bwd(q, k, v, do, True, w.softmax_scale)
+    elif mode == "padded":
+        dq_r, dk_r, dv_r, _, _ = oracle.bwd_mod(q, k, v, do, w.softmax_scale, -1, 0,
+                                                seqlens_k=lens)
     else:
         dq_r, dk_r, dv_r, _, _ = oracle.bwd_mod(q, k, v, do, w.softmax_scale, 80, 20,
                                                 slopes=kw["alibi_slopes"].cpu())
