@@ -54,6 +54,18 @@ def assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     return float(d.max()), float(d.mean()), float(dl.max())
 
 
+def assert_fwd_rows(o, lse, o_r, lse_r, what):
+    """Rows the oracle leaves empty (LSE -inf) must be exactly O = 0, LSE = -inf;
+    the others within the forward tolerance."""
+    o, lse = np64(o), np64(lse)
+    dead = np.isneginf(lse_r)
+    assert np.array_equal(np.isneginf(lse), dead), f"{what}: rows with no key differ"
+    assert np.all(o[dead] == 0.0), f"{what}: O of rows with no key"
+    if (~dead).any():
+        assert_fwd_close(o[~dead], lse[~dead], o_r[~dead], lse_r[~dead], what)
+    return int(dead.sum())
+
+
 def assert_grad_close(g_gpu, g_ref, what=""):
     g = np64(g_gpu) if isinstance(g_gpu, torch.Tensor) else g_gpu
     assert np.all(np.isfinite(g)), f"{what}: non-finite gradient"

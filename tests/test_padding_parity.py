@@ -8,8 +8,8 @@ import torch
 import exact_attention_blackwell_tiled_gb300 as fa
 import oracle
 import synth
-from parity_helpers import (assert_fwd_close, assert_grad_close, check_guards, guarded_empty,
-                            np64)
+from parity_helpers import (assert_fwd_close, assert_fwd_rows, assert_grad_close, check_guards,
+                            guarded_empty, np64)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,18 +52,6 @@ def _inputs(case, seed=41):
 
 def _dev(t):
     return None if t is None else t.to(DEV)
-
-
-def assert_fwd_rows(o, lse, o_r, lse_r, what):
-    """Rows the oracle leaves empty (LSE -inf) must be exactly O = 0, LSE = -inf;
-    the others within the forward tolerance."""
-    o, lse = np64(o), np64(lse)
-    dead = np.isneginf(lse_r)
-    assert np.array_equal(np.isneginf(lse), dead), f"{what}: rows with no key differ"
-    assert np.all(o[dead] == 0.0), f"{what}: O of rows with no key"
-    if (~dead).any():
-        assert_fwd_close(o[~dead], lse[~dead], o_r[~dead], lse_r[~dead], what)
-    return int(dead.sum())
 
 
 @pytest.mark.parametrize("case", CASES, ids=_case_id)
