@@ -465,6 +465,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // (q, dO) fit comfortably in L2
   a.snake = (a.causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
   a.deterministic = deterministic ? 1 : 0;
+  // Head-major dealing with the deterministic mode: each head's tiles are dealt
+  // highest first and the chain adds a block's contributions in that order
+  // (causal tile j reaches a block 2j blocks after its start, so higher tiles
+  // get there first).  The snake keeps ascending order and an ascending chain:
+  // reversed, it would deal the shortest units first and leave a tail.
+  a.desc = (a.deterministic && !a.snake) ? 1 : 0;
   a.dq_groups = groups;
   a.dq_group_stride = (size_t)B * Hq * a.Sq_pad * D;
   a.sem_group_stride = B * Hq * a.n_qblk;

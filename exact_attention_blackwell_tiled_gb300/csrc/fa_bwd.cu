@@ -266,7 +266,34 @@ __device__ __forceinline__ int qblk_first_contributor(int wl, int iq) {
   return wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
 }
 
-// The first kv tile >= first that belongs to deterministic group g.
+template <bool kMod>
+__device__ __forceinline__ bool tile_adds_to(const BwdArgs& a, int j, int kv_len, int iq) {
+  int lo, hi;
+  bwd_qblk_range<kMod>(a, j, kv_len, lo, hi);
+  return lo <= iq && iq < hi;
+}
+
+// The last kv tile that adds into query block iq: the window's bound, cut to
+// the batch's kv tiles, then lowered to a tile whose query-block range really
+// holds iq (the partial tile at the end of the keys, or a tile that starts past
+// the last query but inside its block, can fall short of it).  Called for a
+// block that some tile adds into, so the contiguous run of contributors stops
+// the descent within a step or two.
+template <bool kMod>
+__device__ __forceinline__ int qblk_last_contributor(const BwdArgs& a, int iq, int kv_len) {
+  const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
+  const int n_kt = (kv_len + kTile - 1) / kTile;
+  const int first = qblk_first_contributor(wl, iq);
+  int last = wr >= 0 ? min(n_kt - 1, (iq * kQB + kQB - 1 + wr) / kTile) : n_kt - 1;
+  while (last > first && !tile_adds_to<kMod>(a, last, kv_len, iq)) --last;
+  return last;
+}
+
+// The last kv tile <= last, and the first kv tile >= first, that belong to
+// deterministic group g.
+__device__ __forceinline__ int group_last(int last, int g, int groups) {
+  return last - ((last - g) % groups + groups) % groups;
+}
 __device__ __forceinline__ int group_first(int first, int g, int groups) {
   return first + ((g - first % groups) % groups + groups) % groups;
 }
@@ -373,8 +400,11 @@ struct BwdUnit {
 // head-major (u = bhk * n_ktiles + j, round robin, so CTAs running together
 // share the queries of few heads in L2) or, when those fit in L2 anyway,
 // ordered by ascending kv tile (the longest causal units first) and dealt in a
-// snake so that per-CTA work evens out.  Either order lists kv tile j-1 of a
-// head before tile j, which the deterministic dQ chain relies on.
+// snake so that per-CTA work evens out.  The deterministic dQ chain has each
+// tile wait only for tiles of the same head dealt before it (a CTA waiting on
+// a tile dealt to it later would wait out its timeout): with the snake it runs
+// in ascending tile order; head-major, the deterministic mode deals each
+// head's tiles in descending order (bwd_unit) and chains them that way.
 __device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
   const int k = a.snake ? r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x
                                                          : (int)blockIdx.x)
@@ -396,6 +426,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
   w.b = w.bhk / a.Hkv;
   w.hk = w.bhk - w.b * a.Hkv;
   w.kv_len = bwd_kv_len<kMod>(a, w.b);
+  if (a.desc) w.j = a.n_ktiles - 1 - w.j;  // each head's tiles highest first
   int hi;
   bwd_qblk_range<kMod>(a, w.j, w.kv_len, w.lo, hi);
   w.n_blk = hi - w.lo;
@@ -817,11 +848,17 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           }
         } else {
           // deterministic mode: kv tile j adds into accumulator g = j % G after
-          // the tiles of its group before it (from the block's first
-          // contributor on); the first of them stores instead of adding
-          const int first = qblk_first_contributor(win_left<kMod>(a), iq);
+          // the group's tiles before it in the dealing order, the first of
+          // them storing instead of adding: from the block's first contributor
+          // up (ascending order), or from its last contributor down (each
+          // head's tiles dealt highest first; causal tiles then reach a block
+          // in chain order, tile j starting at block 2j)
           const int g = w.j % a.dq_groups;
-          const int turn = (w.j - group_first(first, g, a.dq_groups)) / a.dq_groups;
+          const int turn =
+              a.desc ? (group_last(qblk_last_contributor<kMod>(a, iq, w.kv_len), g, a.dq_groups) -
+                        w.j) / a.dq_groups
+                     : (w.j - group_first(qblk_first_contributor(win_left<kMod>(a), iq), g,
+                                          a.dq_groups)) / a.dq_groups;
           float* dst = a.dq_acc + (size_t)g * a.dq_group_stride +
                        ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
           int* sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;

@@ -102,6 +102,7 @@ struct BwdArgs {
   int n_ktiles;  // 128-row kv tiles of Sk
   int n_units;
   int snake;     // 1: units dealt longest-first (ascending kv tile) in a snake
+  int desc;      // 1: each head's kv tiles dealt in descending order (deterministic mode)
   // dQ accumulators: 1 in the atomic mode; in the deterministic mode kv tile j
   // adds into accumulator j % dq_groups, chained only behind tile j - dq_groups
   int dq_groups;
