@@ -200,3 +200,18 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fa.fwd(x, x, x)
+
+
+def test_python_binding_checks_score_mod_arrays():
+    """The slopes and key counts must be device arrays of the right type and
+    length; the binding refuses anything else before calling the library."""
+    import torch
+    counts = torch.tensor([3, 4], dtype=torch.int32)  # host memory
+    with pytest.raises(TypeError):
+        fa._score_mod(False, None, None, 2, counts, 2)
+    with pytest.raises(TypeError):
+        fa._score_mod(False, (-1, 0), torch.zeros(2), 2)
+    with pytest.raises(ValueError):
+        fa._score_mod(True, (-1, 0), None, 2)  # the causal flag and a window together
+    # nothing to modify: the plain entry points apply
+    assert fa._score_mod(True, None, None, 2) is None
