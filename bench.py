@@ -1,14 +1,19 @@
 """Throughput benchmark of the fused attention path on GB300.
 
 One step = one training-style pass of the whole hot path over one batch:
-fa_fwd (causal) followed by fa_bwd (causal, atomic dQ) on the training-scale
-workload B=4, Hq=Hkv=16, S=2048, D=128, bf16 (synthetic N(0,1) inputs).
-FLOPs per step follow the measurement convention: 4*B*Hq*Sq*Sk*D forward,
-halved for causal, plus 2.5x that for the backward pass.
+fa_fwd (causal) followed by fa_bwd (causal, atomic dQ) on the largest
+forward + backward workload, B=2, Hq=Hkv=16, S=8192, D=128, bf16 (synthetic
+N(0,1) inputs).  FLOPs per step follow the measurement convention:
+4*B*Hq*Sq*Sk*D forward, halved for causal, plus 2.5x that for the backward
+pass.  The same line also reports, under ``extra``, the training-scale step
+(B=4, H=16, S=2048, causal) measured the same way, and the non-causal D=128
+forward at S = 8k, 16k and 32k (16k tokens per batch).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   torchrun --nproc-per-node N bench.py --gpus N ...   (one rank per GPU)
+  python bench.py --only fwd:S:D:causal --steps K --warmup W
+      (one forward shape alone, for a profiler capture of that kernel)
 
 With N > 1 every rank runs its own batch of the same workload (independent
 units, no collective on the data path); the timing is the max over ranks and
@@ -36,7 +41,10 @@ import synth  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOPs/s (BF16, 1×GB300) and % of tensor-core peak"
 UNIT = "TFLOP/s"
-WORKLOAD = synth.TRAIN  # B=4, Hq=Hkv=16, S=2048, D=128, causal
+WORKLOAD = synth.BWD  # B=2, Hq=Hkv=16, S=8192, D=128, causal: the headline step
+SECONDARY = synth.TRAIN  # B=4, Hq=Hkv=16, S=2048, D=128, causal
+# the forward target: non-causal, D=128, S >= 8k (16k tokens per batch)
+LONG_FWD = [(8192, 128, False), (16384, 128, False), (32768, 128, False)]
 NOMINAL_DENSE_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -75,15 +83,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """DRAM bytes per launch recorded by an ncu capture (profiles/traffic.json),
-    or None when absent or taken on different kernel sources."""
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` recorded by an ncu
+    capture (profiles/traffic.json, keyed "kernel@workload"), or None when
+    absent or taken on different kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel)
+    e = d.get(f"{kernel}@{workload}")
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
     return e.get("bytes_per_launch")
@@ -213,28 +222,15 @@ def cpu_oracle_sample(w: synth.Workload, budget_s: float = 12.0, max_heads: int 
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_ours(args):
+def time_step(fa, w, dev, tensors, steps, warmup, flush, world, stream):
+    """Time W + K fwd+bwd steps (atomic dQ) on workload ``w``, then the forward
+    kernel and the backward main kernel alone (events around each on the
+    launching stream) and the deterministic backward's main kernel.  Returns a
+    dict of per-step / per-kernel times in ms and the launches of the timed
+    steps."""
     import torch
-    import exact_attention_blackwell_tiled_gb300 as fa
-
-    rank, local, world = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    w = WORKLOAD.with_(seed=WORKLOAD.seed + 1000 * rank)  # each rank its own batch
-    q, k, v, do = synth.make_inputs(w, with_do=True)
-    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    qd, kd, vd, dod, o, lse, dq, dk, dv, ws = tensors
     scale = w.softmax_scale
-    o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D), dtype=torch.uint8,
-                     device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     def step(time_kernels=None):
         launches = 0
@@ -249,19 +245,19 @@ def run_ours(args):
         launches += fa.last_launch_count()
         return launches
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
     assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
 
     # Timed region: whole steps bracketed by events, nothing recorded between
     # the kernels (an event there would serialise their programmatic overlap).
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     launches = 0
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()  # L2 flush outside the timed interval
             e = ev[i]
             e[0].record(stream)
@@ -272,7 +268,7 @@ def run_ours(args):
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     # Per-kernel breakdown (the roofline's launch duration): a separate run with
     # events around the forward kernel and the backward main kernel.
-    n_k = min(args.steps, 200)
+    n_k = min(steps, 200)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_k)]
     for i in range(n_k):
         flush.zero_()
@@ -284,20 +280,80 @@ def run_ours(args):
     # the deterministic backward (semaphore-ordered dQ adds), main kernel only
     ws_det = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True),
                          dtype=torch.uint8, device=dev)
-    det_ms = []
-    for i in range(min(args.steps, 50) + 3):
+    det = []
+    for i in range(min(steps, 50) + 3):
         flush.zero_()
         e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         fa.set_timing_events(*e)
         fa.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=scale, workspace=ws_det, dq=dq,
                dk=dk, dv=dv, deterministic=True)
         if i >= 3:
-            det_ms.append(e)
+            det.append(e)
     torch.cuda.synchronize(dev)
     assert fa.bwd_status(ws_det) == fa.FA_OK
-    det_ms = [a.elapsed_time(b) for a, b in det_ms]
+    det_ms = [a.elapsed_time(b) for a, b in det]
     del ws_det
-    total_ms_local = sum(step_ms)
+    return {"step_ms": step_ms, "launches": launches, "clocks": clk.summary(),
+            "fwd_ms": sum(fwd_ms) / len(fwd_ms), "bwd_main_ms": sum(bwd_main_ms) / len(bwd_main_ms),
+            "det_ms": sum(det_ms) / len(det_ms)}
+
+
+def kernel_rates(w, t, peak):
+    """TFLOP/s and fractions of peak of a workload's kernels from time_step()."""
+    fwd_f, bwd_f = w.flops(False), w.flops(True)
+    step_ms = sum(t["step_ms"]) / len(t["step_ms"])
+    fwd_tf = fwd_f / (t["fwd_ms"] * 1e-3) / 1e12
+    bwd_tf = bwd_f / (t["bwd_main_ms"] * 1e-3) / 1e12
+    det_tf = bwd_f / (t["det_ms"] * 1e-3) / 1e12
+    return {"step_tflops": round(step_flops(w) / (step_ms * 1e-3) / 1e12, 1),
+            "ms_per_step": round(step_ms, 4),
+            "fwd_tflops": round(fwd_tf, 1), "fwd_ms": round(t["fwd_ms"], 4),
+            "fwd_frac_of_peak": round(fwd_tf / peak, 4),
+            "bwd_main_tflops": round(bwd_tf, 1), "bwd_main_ms": round(t["bwd_main_ms"], 4),
+            "bwd_main_frac_of_peak": round(bwd_tf / peak, 4),
+            "bwd_main_det_tflops": round(det_tf, 1), "bwd_main_det_ms": round(t["det_ms"], 4),
+            "det_over_atomic": round(t["bwd_main_ms"] / t["det_ms"], 3),
+            "fwd_frac_of_nominal": round(fwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4),
+            "bwd_main_frac_of_nominal": round(bwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4)}
+
+
+def alloc_step(fa, w, dev, rank):
+    """Seeded inputs of workload ``w`` (rank r draws its own batch) on the device,
+    with the outputs and the backward workspace of one step."""
+    import torch
+    w = w.with_(seed=w.seed + 1000 * rank)
+    q, k, v, do = synth.make_inputs(w, with_do=True)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D), dtype=torch.uint8,
+                     device=dev)
+    return (q, k, v, do), (qd, kd, vd, dod, o, lse, dq, dk, dv, ws)
+
+
+def run_ours(args):
+    import torch
+    import exact_attention_blackwell_tiled_gb300 as fa
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if args.only:
+        return run_only(fa, args, dev)
+    w = WORKLOAD
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    host, tensors = alloc_step(fa, w, dev, rank)
+    q, k, v, do = host
+    qd, kd, vd, dod, o, lse, dq, dk, dv, ws = tensors
+    scale = w.softmax_scale
+    t = time_step(fa, w, dev, tensors, args.steps, args.warmup, flush, world, stream)
+    total_ms_local = sum(t["step_ms"])
     total_ms = max_over_ranks(total_ms_local, world, dev)
     ms_per_step = total_ms / args.steps
     flops = step_flops(w)
@@ -305,20 +361,17 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    fwd_f, bwd_f = w.flops(False), w.flops(True)
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    bwd_avg = sum(bwd_main_ms) / len(bwd_main_ms)
-    bwd_tf = bwd_f / (bwd_avg * 1e-3) / 1e12
-    fwd_tf = fwd_f / (fwd_avg * 1e-3) / 1e12
-    if bwd_avg >= fwd_avg:
-        dom, dom_tf, dom_flops = "bwd_main<128>", bwd_tf, bwd_f
+    rates = kernel_rates(w, t, peak)
+    if t["bwd_main_ms"] >= t["fwd_ms"]:
+        dom, dom_ms, dom_flops = "bwd_main<128>", t["bwd_main_ms"], w.flops(True)
     else:
-        dom, dom_tf, dom_flops = "fwd_kernel<128>", fwd_tf, fwd_f
+        dom, dom_ms, dom_flops = "fwd_kernel<128>", t["fwd_ms"], w.flops(False)
+    dom_tf = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(dom_tf, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(dom_tf / peak, 4), "traffic": profiled_traffic(dom),
+                "frac": round(dom_tf / peak, 4), "traffic": profiled_traffic(dom, w.name),
                 "kernel": dom, "flops_per_launch": dom_flops,
                 "peak_source": f"bf16_tflops burst, {peak_src}"}
-    clocks = clk.summary()
+    clocks = t["clocks"]
 
     # End to end through the public API: every step copies its inputs from
     # pinned host memory, runs fwd + bwd and copies the gradients back.  As in a
@@ -327,10 +380,10 @@ def run_ours(args):
     # download overlap step i's compute; all of them lie inside the timed region.
     e2e = None
     if rank == 0 or world > 1:
-        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
-        out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
-        ins = [[torch.empty_like(t) for t in (qd, kd, vd, dod)] for _ in range(2)]
-        outs = [[torch.empty_like(t) for t in (qd, kd, vd)] for _ in range(2)]
+        hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, do))
+        out_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, k, v)]
+        ins = [[torch.empty_like(x) for x in (qd, kd, vd, dod)] for _ in range(2)]
+        outs = [[torch.empty_like(x) for x in (qd, kd, vd)] for _ in range(2)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -381,27 +434,35 @@ def run_ours(args):
         t_e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(t_e0.elapsed_time(t_e1) / n_e2e, world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
-        d2h = sum(t.numel() * t.element_size() for t in out_h)
+        h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do))
+        d2h = sum(x.numel() * x.element_size() for x in out_h)
         e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4),
                "overlap": "upload of step i+1 and download of step i-1 overlap step i"}
-        del ins, outs
+        del ins, outs, hq, hk, hv, hdo, out_h
 
     assert fa.fwd_status() == fa.FA_OK and fa.bwd_status(ws) == fa.FA_OK
+    del host, tensors, qd, kd, vd, dod, o, lse, dq, dk, dv, ws
 
-    extra = {"fwd_tflops": round(fwd_tf, 1), "fwd_ms": round(fwd_avg, 4),
-             "bwd_main_tflops": round(bwd_tf, 1), "bwd_main_ms": round(bwd_avg, 4),
-             "bwd_main_det_tflops": round(bwd_f / (sum(det_ms) / len(det_ms) * 1e-3) / 1e12, 1),
-             "det_over_atomic": round(bwd_avg / (sum(det_ms) / len(det_ms)), 3),
-             "bwd_total_flops_tflops_incl_pre_post": None,
-             "fwd_frac_of_peak": round(fwd_tf / peak, 4), "peak_tflops": peak,
-             # the vendor's dense bf16 figure for one GB300 (2.25 PFLOP/s without
-             # sparsity), the like-for-like denominator of a "% of theoretical peak"
-             "nominal_dense_bf16_tflops": NOMINAL_DENSE_BF16_TFLOPS,
-             "fwd_frac_of_nominal": round(fwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4),
-             "bwd_main_frac_of_nominal": round(bwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4)}
+    extra = dict(rates)
+    extra["peak_tflops"] = peak
+    # the vendor's dense bf16 figure for one GB300 (2.25 PFLOP/s without
+    # sparsity), the like-for-like denominator of a "% of theoretical peak"
+    extra["nominal_dense_bf16_tflops"] = NOMINAL_DENSE_BF16_TFLOPS
+    # the training-scale step (B=4, H=16, S=2048, causal), measured the same way
+    if not args.no_train_step:
+        w2 = SECONDARY
+        _, tensors2 = alloc_step(fa, w2, dev, rank)
+        t2 = time_step(fa, w2, dev, tensors2, args.steps, args.warmup, flush, world, stream)
+        r2 = kernel_rates(w2, t2, peak)
+        r2["workload"] = config_dict(w2)["workload"]
+        r2["traffic_bwd_main"] = profiled_traffic("bwd_main<128>", w2.name)
+        extra["train_step"] = r2
+        del tensors2
+    # the forward target: non-causal D=128 at S >= 8k (16k tokens per batch)
+    if rank == 0 and not args.no_long_fwd:
+        extra["fwd_noncausal_long"] = fwd_sweep(fa, dev, peak, shapes=LONG_FWD)
     if args.sweep and rank == 0:
         extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
     if args.mod_sweep and rank == 0:
@@ -424,37 +485,67 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
             "config": config_dict(w), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks, "extra": extra}
+            "gpu_launches": t["launches"], "clocks": clocks, "extra": extra}
     print(json.dumps(line), flush=True)
 
 
-def fwd_sweep(fa, dev, peak, iters=10):
-    """Forward-only TFLOP/s over the sequence-length sweep (16k tokens per batch)."""
+def run_only(fa, args, dev):
+    """One forward shape alone (``--only fwd:S:D:causal``): W + K launches of the
+    forward kernel on the sweep workload of that S and D, nothing else -- the
+    command a profiler capture of that kernel runs."""
+    import torch
+    kind, S, D, c = args.only.split(":")
+    if kind != "fwd":
+        raise SystemExit(f"--only: unknown kind {kind!r}")
+    w = synth.sweep(int(S), int(D), c in ("1", "c", "causal", "true"))
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    q, k, v = (torch.randn(w.B, w.Hq, w.Sq, w.D, device=dev, generator=gen).to(torch.bfloat16)
+               for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    ev = []
+    for i in range(args.warmup + args.steps):
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        fa.set_timing_events(*e)
+        fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+        if i >= args.warmup:
+            ev.append(e)
+    torch.cuda.synchronize(dev)
+    assert fa.fwd_status() == fa.FA_OK
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+    print(json.dumps({"only": args.only, "workload": w.name, "B": w.B, "H": w.Hq, "S": w.Sq,
+                      "D": w.D, "causal": w.causal, "ms": round(ms, 4),
+                      "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1)}), flush=True)
+
+
+def fwd_sweep(fa, dev, peak, iters=10, shapes=None):
+    """Forward-only TFLOP/s over the sequence-length sweep (16k tokens per batch),
+    or over ``shapes`` [(S, D, causal), ...] of it."""
     import torch
     out = []
-    for S in synth.SWEEP_S:
-        for D in (64, 128):
-            for causal in (False, True):
-                w = synth.sweep(S, D, causal)
-                q, k, v = (torch.randn(w.B, w.Hq, S, D, device=dev, dtype=torch.bfloat16)
-                           for _ in range(3))
-                o = torch.empty_like(q)
-                lse = torch.empty((w.B, w.Hq, S), dtype=torch.float32, device=dev)
-                for _ in range(3):
-                    fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
-                torch.cuda.synchronize(dev)
-                t = []
-                for _ in range(iters):
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    fa.set_timing_events(e0, e1)
-                    fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
-                    t.append((e0, e1))
-                torch.cuda.synchronize(dev)
-                ms = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
-                tf = w.flops() / (ms * 1e-3) / 1e12
-                out.append({"S": S, "D": D, "B": w.B, "causal": causal, "ms": round(ms, 4),
-                            "tflops": round(tf, 1), "frac": round(tf / peak, 4)})
-                del q, k, v, o, lse
+    if shapes is None:
+        shapes = [(S, D, c) for S in synth.SWEEP_S for D in (64, 128) for c in (False, True)]
+    for S, D, causal in shapes:
+        w = synth.sweep(S, D, causal)
+        q, k, v = (torch.randn(w.B, w.Hq, S, D, device=dev, dtype=torch.bfloat16)
+                   for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, S), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        torch.cuda.synchronize(dev)
+        t = []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fa.set_timing_events(e0, e1)
+            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+            t.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in t)[len(t) // 2]
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        out.append({"S": S, "D": D, "B": w.B, "causal": causal, "ms": round(ms, 4),
+                    "tflops": round(tf, 1), "frac": round(tf / peak, 4)})
+        del q, k, v, o, lse
     return out
 
 
@@ -659,6 +750,12 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for the baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train-step", action="store_true",
+                    help="skip the training-scale step reported under extra")
+    ap.add_argument("--no-long-fwd", action="store_true",
+                    help="skip the non-causal S >= 8k forward reported under extra")
+    ap.add_argument("--only", default=None,
+                    help="fwd:S:D:causal -- time one forward shape alone and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -95,6 +95,41 @@ def test_deterministic_is_bit_identical():
             assert torch.equal(a, b), "deterministic backward differs between runs"
 
 
+def _qdo_bytes(w: synth.Workload) -> int:
+    return 2 * w.B * w.Hq * w.Sq * w.D * 2
+
+
+DET_WORKLOADS = [
+    # the training-scale step: q and dO fit in 64 MiB, units dealt longest
+    # first in a snake, each block's chain ascending over the kv tiles
+    (synth.TRAIN.with_(with_do=True), True),
+    # the backward workload: head-major dealing, chains descending
+    (synth.BWD, False),
+    (synth.BWD.with_(name="bwd_noncausal", causal=False), False),
+]
+
+
+@pytest.mark.parametrize("w,snake", DET_WORKLOADS, ids=lambda x: getattr(x, "name", ""))
+def test_deterministic_bit_identical_at_workload_size(w, snake):
+    """The deterministic backward gives the same bits on five runs at full
+    workload size, on both chain orders."""
+    assert (w.causal and _qdo_bytes(w) <= 64 << 20) == snake, "dealing order changed"
+    q, k, v, do = (t.to(DEV) for t in synth.make_inputs(w, with_do=True))
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.softmax_scale)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True),
+                     dtype=torch.uint8, device=DEV)
+    first = fa.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.softmax_scale,
+                   deterministic=True, workspace=ws)
+    first = [t.clone() for t in first]
+    assert fa.bwd_status(ws) == fa.FA_OK
+    for run in range(4):
+        again = fa.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.softmax_scale,
+                       deterministic=True, workspace=ws)
+        assert fa.bwd_status(ws) == fa.FA_OK
+        for name, a, b in zip(("dQ", "dK", "dV"), first, again):
+            assert torch.equal(a, b), f"{w.name}: deterministic {name} differs on run {run + 2}"
+
+
 def test_bwd_workload_sampled_heads():
     """The backward workload (B=2, H=16, S=8192, D=128, causal) at full size;
     two kv heads are checked against the full fp64 backward, every output is

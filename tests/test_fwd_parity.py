@@ -94,7 +94,7 @@ def test_forward_is_deterministic():
 
 
 def _sampled(w: synth.Workload, n_per_head, full_heads):
-    q, k, v = synth.make_inputs(w)
+    q, k, v = synth.make_inputs(w, with_do=False)
     qd, kd, vd = (t.to(DEV) for t in (q, k, v))
     o, lse = fa.fwd(qd, kd, vd, causal=w.causal, scale=w.softmax_scale)
     torch.cuda.synchronize()
@@ -126,6 +126,32 @@ def test_gqa_spike_sampled():
                                         (16384, 64, True), (32768, 128, False)])
 def test_sweep_sampled(S, D, causal):
     _sampled(synth.sweep(S, D, causal), 16 if S >= 16384 else 48, 0)
+
+
+def _kv_bytes(w: synth.Workload) -> int:
+    return 2 * w.B * w.Hkv * w.Sk * w.D * 2
+
+
+@pytest.mark.parametrize("S", [1024, 2048, 32768])
+def test_sweep_causal_d128_chunked(S):
+    """Causal D=128 sweep points.  Their K/V exceed 64 MiB, so the forward deals
+    each CTA a contiguous chunk of head-major units, a long and a short tile
+    pair of a head together (the chunked causal schedule); at S=32768 the 2048
+    units make 146 chunks of 14 and a last chunk of 4.  Sampled rows of every
+    head and two whole heads against the oracle."""
+    w = synth.sweep(S, 128, True)
+    assert _kv_bytes(w) > 64 << 20, "this shape no longer takes the chunked schedule"
+    _sampled(w, 32, 2)
+
+
+def test_bwd_workload_forward_sampled():
+    """The forward of the backward workload (B=2, H=16, S=8192, D=128, causal),
+    which gives the backward its O and LSE: K/V of 128 MiB, the chunked causal
+    schedule.  O and LSE checked on sampled rows of every head and two whole
+    heads."""
+    w = synth.BWD
+    assert _kv_bytes(w) > 64 << 20
+    _sampled(w, 32, 2)
 
 
 def test_timing_events_bracket_the_kernel():

@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
         bench.barrier(world)
         # every rank draws its own batch: different seeds give different data
         wl = bench.WORKLOAD.with_(B=1, Sq=64, Sk=64, seed=bench.WORKLOAD.seed + 1000 * rank)
-        q, _, _ = synth.make_inputs(wl)
+        q = synth.make_inputs(wl)[0]
         gathered = [torch.zeros_like(q) for _ in range(world)]
         dist.all_gather(gathered, q.float().to(torch.bfloat16))
         distinct = not torch.equal(gathered[0], gathered[1])
@@ -76,7 +76,7 @@ def test_weak_scaling_value_arithmetic():
     """value = FLOPs of all ranks / max-over-ranks time."""
     w = bench.WORKLOAD
     f = bench.step_flops(w)
-    assert f == pytest.approx(3.5 * 4 * 4 * 16 * 2048 * 2048 * 128 * 0.5)
+    assert f == pytest.approx(3.5 * 4 * 2 * 16 * 8192 * 8192 * 128 * 0.5)
     steps, world, total_ms = 10, 4, 5.0
     value = f * world * steps / (total_ms * 1e-3) / 1e12
     assert value == pytest.approx(4 * 10 * f / 5e-3 / 1e12)
