@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa.so")
 
 FA_OK = 0
+FA_ERR_WORKSPACE = 4
 FA_ERR_TIMEOUT = 6
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA",
@@ -27,7 +28,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
            "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
            "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod", "fa_fwd_split_count",
-           "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge", "fa_wait_test")
+           "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge", "fa_wait_test",
+           "fa_bwd_noalloc_status")
 
 
 class ScoreMod(ctypes.Structure):
@@ -71,6 +73,8 @@ def _bind(lib):
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i,
                                    vp]
     lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc_status.argtypes = [vp]
+    lib.fa_bwd_noalloc_status.restype = i
     smp = ctypes.POINTER(ScoreMod)
     lib.fa_fwd_mod.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, smp, f, vp]
     lib.fa_fwd_mod.restype = i

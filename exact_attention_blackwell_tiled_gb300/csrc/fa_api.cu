@@ -427,10 +427,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   const void* do_map = has_q ? dO : k;
   const int bh_map = has_q ? B * Hq : B * Hkv;
   const int sq_map = has_q ? Sq : Sk;
-  // q and dO move in 64-row blocks in the backward pass
-  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D, 64) ||
+  // q and dO move in blocks of bwd_qblk_rows rows in the backward pass
+  const int qrows = bwd_qblk_rows(D, deterministic);
+  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D, qrows) ||
       !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) || !make_tmap_bsd(&tv, v, B * Hkv, Sk, D) ||
-      !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D, 64))
+      !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D, qrows))
     return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdArgs a{};
@@ -474,6 +475,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.dq_groups = groups;
   a.dq_group_stride = (size_t)B * Hq * a.Sq_pad * D;
   a.sem_group_stride = B * Hq * a.n_qblk;
+  a.qblk_rows = qrows;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));

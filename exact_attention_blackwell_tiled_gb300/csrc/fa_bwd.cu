@@ -71,6 +71,7 @@
 
 #include <climits>
 
+#include "bwd_common.cuh"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -218,222 +219,6 @@ struct BwdSmem {
                             kColDK = 256 + D;
 };
 
-// The window (wl, wr) a kernel instantiation applies: kMod reads it from the
-// arguments, the plain kernel has none or the causal one.
-template <bool kMod>
-__device__ __forceinline__ int win_left(const BwdArgs& a) {
-  return kMod ? a.wl : -1;
-}
-template <bool kMod>
-__device__ __forceinline__ int win_right(const BwdArgs& a) {
-  return kMod ? a.wr : (a.causal ? 0 : -1);
-}
-
-// Keys of batch b that exist: seqlens_k[b] clamped to [0, Sk] (the key padding
-// mask); all Sk without lengths, and always in the plain kernel.
-template <bool kMod>
-__device__ __forceinline__ int bwd_kv_len(const BwdArgs& a, int b) {
-  if (!kMod || !a.seqlens_k) return a.Sk;
-  const int n = __ldg(a.seqlens_k + b);
-  return n < 0 ? 0 : (n < a.Sk ? n : a.Sk);
-}
-
-// 64-row query blocks [lo, hi) with a query that sees a key of kv tile j (of a
-// batch with kv_len keys): the queries from (first key - wr) to (last key +
-// wl); empty when the tile holds no key of the batch
-template <bool kMod>
-__device__ __forceinline__ void bwd_qblk_range(const BwdArgs& a, int j, int kv_len, int& lo,
-                                               int& hi) {
-  const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
-  const int k0 = j * kTile;
-  if (k0 >= kv_len) {
-    lo = hi = 0;
-    return;
-  }
-  const int k1 = min(kv_len, k0 + kTile) - 1;
-  const int q_lo = wr >= 0 ? max(0, k0 - wr) : 0;
-  const int q_hi = wl >= 0 ? min(a.Sq - 1, k1 + wl) : a.Sq - 1;
-  lo = q_lo / kQB;
-  hi = q_hi >= q_lo ? q_hi / kQB + 1 : lo;
-}
-
-// The first kv tile that adds into 64-row query block iq: the kv tiles that do
-// (those whose bwd_qblk_range holds iq) are a contiguous run, since both ends
-// of that range grow with j, and the run starts at the first tile whose last
-// key reaches the block's first query - wl.  (The bound can overshoot only when
-// no tile adds at all, which a caller that adds never meets.)
-__device__ __forceinline__ int qblk_first_contributor(int wl, int iq) {
-  return wl >= 0 ? max(0, iq * kQB - wl) / kTile : 0;
-}
-
-template <bool kMod>
-__device__ __forceinline__ bool tile_adds_to(const BwdArgs& a, int j, int kv_len, int iq) {
-  int lo, hi;
-  bwd_qblk_range<kMod>(a, j, kv_len, lo, hi);
-  return lo <= iq && iq < hi;
-}
-
-// The last kv tile that adds into query block iq: the window's bound, cut to
-// the batch's kv tiles, then lowered to a tile whose query-block range really
-// holds iq (the partial tile at the end of the keys, or a tile that starts past
-// the last query but inside its block, can fall short of it).  Called for a
-// block that some tile adds into, so the contiguous run of contributors stops
-// the descent within a step or two.
-template <bool kMod>
-__device__ __forceinline__ int qblk_last_contributor(const BwdArgs& a, int iq, int kv_len) {
-  const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
-  const int n_kt = (kv_len + kTile - 1) / kTile;
-  const int first = qblk_first_contributor(wl, iq);
-  int last = wr >= 0 ? min(n_kt - 1, (iq * kQB + kQB - 1 + wr) / kTile) : n_kt - 1;
-  while (last > first && !tile_adds_to<kMod>(a, last, kv_len, iq)) --last;
-  return last;
-}
-
-// The last kv tile <= last, and the first kv tile >= first, that belong to
-// deterministic group g.
-__device__ __forceinline__ int group_last(int last, int g, int groups) {
-  return last - ((last - g) % groups + groups) % groups;
-}
-__device__ __forceinline__ int group_first(int first, int g, int groups) {
-  return first + ((g - first % groups) % groups + groups) % groups;
-}
-
-__device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// AND of `ok` over the 128 threads of a warpgroup (named barrier `id`); every
-// thread of the group must call it the same number of times.
-__device__ __forceinline__ bool group_all(bool ok, int id) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.and.pred q, %2, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "r"(id)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
-}
-
-__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
-  }
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// n consecutive 32-bit columns of this thread's lane (n = 8, 16, 32), waited.
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
-  static_assert(N == 16 || N == 32, "tmem_ld width");
-  if constexpr (N == 32) {
-    tmem_ld32(taddr, r);
-  } else {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-  }
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]);
-
-// Writes n consecutive 32-bit columns of this thread's lane (no wait).
-template <int N>
-__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&w)[N]) {
-  static_assert(N == 8 || N == 16, "tmem_st width");
-  if constexpr (N == 16) {
-    tmem_st16(taddr, w);
-  } else {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-            taddr),
-        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-        : "memory");
-  }
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
-      "r"(w[15])
-      : "memory");
-}
-
-// Iterations (q head of the group x query block) of kv tile j.
-struct BwdUnit {
-  int bhk, j, b, hk, lo, n_blk, n_it;
-  int kv_len;  // keys of batch b
-};
-
-// The r-th unit this CTA processes (-1 when it has no more).  Units are either
-// head-major (u = bhk * n_ktiles + j, round robin, so CTAs running together
-// share the queries of few heads in L2) or, when those fit in L2 anyway,
-// ordered by ascending kv tile (the longest causal units first) and dealt in a
-// snake so that per-CTA work evens out.  The deterministic dQ chain has each
-// tile wait only for tiles of the same head dealt before it (a CTA waiting on
-// a tile dealt to it later would wait out its timeout): with the snake it runs
-// in ascending tile order; head-major, the deterministic mode deals each
-// head's tiles in descending order (bwd_unit) and chains them that way.
-__device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
-  const int k = a.snake ? r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x
-                                                         : (int)blockIdx.x)
-                        : (int)blockIdx.x + r * (int)gridDim.x;
-  return k < a.n_units ? k : -1;
-}
-
-template <bool kMod>
-__device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) {
-  BwdUnit w;
-  if (a.snake) {
-    const int nbhk = a.B * a.Hkv;
-    w.j = u / nbhk;
-    w.bhk = u - w.j * nbhk;
-  } else {
-    w.bhk = u / a.n_ktiles;
-    w.j = u - w.bhk * a.n_ktiles;
-  }
-  w.b = w.bhk / a.Hkv;
-  w.hk = w.bhk - w.b * a.Hkv;
-  w.kv_len = bwd_kv_len<kMod>(a, w.b);
-  if (a.desc) w.j = a.n_ktiles - 1 - w.j;  // each head's tiles highest first
-  int hi;
-  bwd_qblk_range<kMod>(a, w.j, w.kv_len, w.lo, hi);
-  w.n_blk = hi - w.lo;
-  w.n_it = group * w.n_blk;
-  return w;
-}
-
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
 // plain kernel applies no mask or the causal one.
 template <int D, bool kMod>
@@ -517,7 +302,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         return true;
       };
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit<kMod>(a, u, group);
+        const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
         // The unit's first block's Q / dO go out before its K / V: its stage
         // frees up while the previous unit still holds K and V, so it has landed
         // by the time K and V can be replaced.  Later blocks follow K and V, which
@@ -569,7 +354,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit<kMod>(a, u, group);
+        const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (role < 2) {
@@ -705,7 +490,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
-      const BwdUnit w = bwd_unit<kMod>(a, u, group);
+      const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= w.kv_len;
       for (int t = 0; t < w.n_it; ++t, ++it) {
@@ -812,7 +597,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     uint32_t it = 0, unit = 0;
     bool ok = true;
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-      const BwdUnit w = bwd_unit<kMod>(a, u, group);
+      const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
@@ -855,9 +640,9 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           // in chain order, tile j starting at block 2j)
           const int g = w.j % a.dq_groups;
           const int turn =
-              a.desc ? (group_last(qblk_last_contributor<kMod>(a, iq, w.kv_len), g, a.dq_groups) -
+              a.desc ? (group_last(qblk_last_contributor<kMod, kQB>(a, iq, w.kv_len), g, a.dq_groups) -
                         w.j) / a.dq_groups
-                     : (w.j - group_first(qblk_first_contributor(win_left<kMod>(a), iq), g,
+                     : (w.j - group_first(qblk_first_contributor<kQB>(win_left<kMod>(a), iq), g,
                                           a.dq_groups)) / a.dq_groups;
           float* dst = a.dq_acc + (size_t)g * a.dq_group_stride +
                        ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
@@ -997,7 +782,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
       // the groups' accumulators in fixed order; a group that no kv tile
       // wrote for this query block (its semaphore, the count of warps that
       // added, is 0) holds stale memory and is skipped
-      const int* sem = a.sem + (size_t)bh * a.n_qblk + i / kQB;
+      const int* sem = a.sem + (size_t)bh * a.n_qblk + i / (uint32_t)a.qblk_rows;
       if (__ldg(sem) == 0) x0 = x1 = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int g = 1; g < a.dq_groups; ++g) {
         if (__ldg(sem + (size_t)g * a.sem_group_stride) == 0) continue;
@@ -1055,7 +840,10 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     const int threads =
         (mod || D == 64) ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;
     record_timing(false, stream);
-    if (a.deterministic) {
+    if (a.qblk_rows == 128) {
+      const int rc = launch_bwd_main_q128(tq, tk, tv, tdo, a, mod, grid, stream);
+      if (rc != FA_OK) return rc;
+    } else if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
       cfg.blockDim = dim3(threads);

@@ -108,6 +108,8 @@ struct BwdArgs {
   int dq_groups;
   size_t dq_group_stride;  // floats from one accumulator to the next
   int sem_group_stride;    // semaphores from one group to the next
+  int qblk_rows;           // query rows per block of the main kernel (64 or 128):
+                           // semaphore i of a head counts the writers of block i
 };
 
 constexpr int kDetGroups = 4;  // deterministic-mode accumulators (at most)
@@ -125,6 +127,23 @@ bool bwd_layout(int B, int Hq, int Sq, int D, int groups, BwdLayout* L);
 
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+
+// The backward's query rows per block: 128 (bwd_main_q128) for the
+// deterministic mode at D = 128, 64 (bwd_main) otherwise.  The q and dO tensor
+// maps use boxes of this many rows.  Measured on GB300: with atomic dQ adds
+// both kernels are bound by the fp32 reduction traffic into L2 (4.4 GB per
+// backward at B2 H16 S8192 causal, 3.4-3.6 TB/s either way), where the 64-row
+// kernel's adds interfere less with its softmax warps; the deterministic mode,
+// which stores a quarter of its contributions, runs 1.2-1.45x faster with
+// 128-row blocks.
+inline int bwd_qblk_rows(int D, int deterministic) {
+  return (D == 128 && deterministic) ? 128 : 64;
+}
+
+// Main kernel of the 128-row-block backward (D = 128 only).
+int launch_bwd_main_q128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdArgs& a, bool mod, int grid,
+                         cudaStream_t stream);
 
 void note_launches(int n);
 

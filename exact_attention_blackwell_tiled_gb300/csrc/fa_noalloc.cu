@@ -14,7 +14,9 @@
 // Host code cannot use the array's name as a device pointer: on the host it only
 // stands for the symbol.  The device address is therefore looked up once per
 // device with cudaGetSymbolAddress (on the first call made with that device
-// current) and cached.
+// current) and cached.  The cache is not refreshed: after cudaDeviceReset the
+// device's context is a new one and the cached address is stale, so these
+// entry points must not be used across a reset of the device.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -64,4 +66,13 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   // call left in the scratch does not matter.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, causal, scale, scratch,
                 fa::kNoAllocScratchBytes, deterministic, stream);
+}
+
+// The status word sits at the start of the scratch, where fa_bwd keeps it in
+// any workspace; reading it is a small device-to-host copy into a local
+// variable, which allocates nothing either.
+extern "C" int fa_bwd_noalloc_status(fa_stream_t stream) {
+  void* scratch = fa::scratch_address();
+  if (scratch == nullptr) return FA_ERR_CUDA;
+  return fa_bwd_status(scratch, stream);
 }

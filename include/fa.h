@@ -286,12 +286,25 @@ int fa_set_timing_events(void* start_event, void* stop_event);
  *     contents; each call clears what it needs cleared.  Calls that overlap on
  *     the GPU (different streams, or different host threads without ordering)
  *     race on it and produce wrong gradients: serialise them.
- *   - Device-side timeouts are recorded in the scratch and cannot be read back
- *     through fa_bwd_status.
+ *   - A device-side wait that runs out is recorded in the scratch's status
+ *     word; fa_bwd_noalloc_status reads it back.
+ *   - The scratch's address is looked up once per device and kept, so the
+ *     entry points must not be used across cudaDeviceReset of that device.
  */
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                    const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
                    int Sk, int D, int causal, float scale, int deterministic, fa_stream_t stream);
+
+/*
+ * Status of the last fa_bwd_noalloc on the current device (the pages have no
+ * counterpart; this is the no-allocation form of fa_bwd_status).  Synchronises
+ * `stream` (pass the stream of the fa_bwd_noalloc call), then returns FA_OK or
+ * FA_ERR_TIMEOUT from the status word in the built-in scratch; FA_ERR_CUDA if
+ * the synchronisation, the address lookup or the read fails.  Allocates
+ * nothing.  Each fa_bwd_noalloc clears the word, so the status is that of the
+ * latest call.
+ */
+int fa_bwd_noalloc_status(fa_stream_t stream);
 
 #ifdef __cplusplus
 }
