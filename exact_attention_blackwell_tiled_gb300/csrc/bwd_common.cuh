@@ -192,9 +192,9 @@ struct BwdUnit {
 
 // The r-th unit this CTA processes (-1 when it has no more).  Units are either
 // head-major (u = bhk * n_ktiles + j, round robin, so CTAs running together
-// share the queries of few heads in L2) or, when those fit in L2 anyway,
-// ordered by ascending kv tile (the longest causal units first) and dealt in a
-// snake so that per-CTA work evens out.  The deterministic dQ chain has each
+// share the queries of few heads in L2; non-causal and windowed calls) or,
+// with causal masking, ordered by ascending kv tile (the longest units first)
+// and dealt in a snake so that per-CTA work evens out.  The deterministic dQ chain has each
 // tile wait only for tiles of the same head dealt before it (a CTA waiting on
 // a tile dealt to it later would wait out its timeout): with the snake it runs
 // in ascending tile order; head-major, the deterministic mode deals each
@@ -203,6 +203,16 @@ __device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
   const int k = a.snake ? r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x
                                                          : (int)blockIdx.x)
                         : (int)blockIdx.x + r * (int)gridDim.x;
+  return k < a.n_units ? k : -1;
+}
+
+// The same dealing over clusters of two CTAs (kPair): both CTAs of cluster c =
+// blockIdx.x / 2 walk the same pair units.
+template <bool kPair>
+__device__ __forceinline__ int bwd_cta_unit_p(const BwdArgs& a, int r) {
+  if (!kPair) return bwd_cta_unit(a, r);
+  const int id = (int)(blockIdx.x >> 1), n = (int)(gridDim.x >> 1);
+  const int k = a.snake ? r * n + ((r & 1) ? n - 1 - id : id) : id + r * n;
   return k < a.n_units ? k : -1;
 }
 
@@ -226,6 +236,111 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) 
   w.n_blk = hi - w.lo;
   w.n_it = group * w.n_blk;
   return w;
+}
+
+// Pair unit u of a cluster of two CTAs: (batch, kv head, kv tiles 2p and 2p+1);
+// the CTA of cluster rank `rank` takes tile 2p + rank (a tile past the last one
+// holds no key).  Both CTAs walk the union of the two tiles' query-block
+// ranges, so that they meet every block together for the dQ exchange; a block
+// outside a tile's own range is fully masked for it and adds nothing.
+template <bool kMod, int QB>
+__device__ __forceinline__ BwdUnit bwd_unit_pair(const BwdArgs& a, int u, int group, int rank) {
+  BwdUnit w;
+  const int n_jp = (a.n_ktiles + 1) / 2;
+  int jp;
+  if (a.snake) {
+    const int nbhk = a.B * a.Hkv;
+    jp = u / nbhk;
+    w.bhk = u - jp * nbhk;
+  } else {
+    w.bhk = u / n_jp;
+    jp = u - w.bhk * n_jp;
+  }
+  w.b = w.bhk / a.Hkv;
+  w.hk = w.bhk - w.b * a.Hkv;
+  w.kv_len = bwd_kv_len<kMod>(a, w.b);
+  w.j = 2 * jp + rank;
+  int lo0, hi0, lo1 = 0, hi1 = 0;
+  bwd_qblk_range<kMod, QB>(a, 2 * jp, w.kv_len, lo0, hi0);
+  if (2 * jp + 1 < a.n_ktiles) bwd_qblk_range<kMod, QB>(a, 2 * jp + 1, w.kv_len, lo1, hi1);
+  int lo, hi;
+  if (hi0 <= lo0) {
+    lo = lo1, hi = hi1;
+  } else if (hi1 <= lo1) {
+    lo = lo0, hi = hi0;
+  } else {
+    lo = min(lo0, lo1), hi = max(hi0, hi1);
+  }
+  w.lo = lo;
+  w.n_blk = hi > lo ? hi - lo : 0;
+  w.n_it = group * w.n_blk;
+  return w;
+}
+
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs of the cluster; release / acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of this CTA's shared address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrives once on the mbarrier at shared::cluster address `remote_bar`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
+// Stores 4 bytes into another CTA's shared memory; the write counts 4 bytes of
+// transaction on the mbarrier at `remote_bar` (same CTA as `remote_addr`).
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+      "r"(v), "r"(remote_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on a local mbarrier that another CTA of the cluster completes
+// (acquire at cluster scope); gives up like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
 }
 
 }  // namespace fa

@@ -462,15 +462,17 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.wr = m.wr;
   a.alibi = has_q ? m.alibi : nullptr;
   a.seqlens_k = has_q ? m.seqlens_k : nullptr;  // with no queries dK = dV = 0 anyway
-  // longest-first snake when the streamed queries and output gradients
-  // (q, dO) fit comfortably in L2
-  a.snake = (a.causal && 2.0 * B * Hq * (double)Sq * D * 2 <= 64.0 * (1 << 20)) ? 1 : 0;
+  // causal: longest-first snake over all heads.  Also when q and dO exceed L2:
+  // measured on GB300 against head-major dealing at B2 H16 S8192 (q, dO 128
+  // MiB), the main kernel ran 1,011 -> 1,189 TFLOP/s with atomic dQ and
+  // 594 -> 664 in the deterministic mode
+  a.snake = a.causal ? 1 : 0;
   a.deterministic = deterministic ? 1 : 0;
-  // Head-major dealing with the deterministic mode: each head's tiles are dealt
-  // highest first and the chain adds a block's contributions in that order
-  // (causal tile j reaches a block 2j blocks after its start, so higher tiles
-  // get there first).  The snake keeps ascending order and an ascending chain:
-  // reversed, it would deal the shortest units first and leave a tail.
+  // Head-major dealing (non-causal and windowed calls) with the deterministic
+  // mode: each head's tiles are dealt highest first and the chain adds a
+  // block's contributions in that order.  The snake keeps ascending order and
+  // an ascending chain: reversed, it would deal the shortest units first and
+  // leave a tail.
   a.desc = (a.deterministic && !a.snake) ? 1 : 0;
   a.dq_groups = groups;
   a.dq_group_stride = (size_t)B * Hq * a.Sq_pad * D;

@@ -210,7 +210,11 @@ struct BwdSmem {
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
   static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
-  static constexpr int kNumBars = kBarDrain + 3;
+  // CTA pairs (atomic dQ at D = 128): the partner's stage is free to receive
+  // (arrived by the partner), and the partner's dQ^T rows have arrived (tx)
+  static constexpr int kBarPeerReady = kBarDrain + 3;
+  static constexpr int kBarRecvFull = kBarPeerReady + 1;
+  static constexpr int kNumBars = kBarRecvFull + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
@@ -220,14 +224,22 @@ struct BwdSmem {
 };
 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
-// plain kernel applies no mask or the causal one.
-template <int D, bool kMod>
+// plain kernel applies no mask or the causal one.  kPair (atomic dQ, D = 128):
+// clusters of two CTAs take adjacent kv tiles 2p, 2p+1 of one head and walk
+// the same query blocks; per block each CTA keeps 64 head-dim rows of dQ^T,
+// receives the partner's partial of those rows into the block's stage (whose
+// Q / dO the MMAs have finished with) through distributed shared memory,
+// and adds the sum: the pair reduces over 256 keys before the global adds,
+// which halves the fp32 reduction traffic into L2 (FlashAttention-4 pages,
+// key contribution #3: a restructured dQ reduction with half the atomic adds).
+template <int D, bool kMod, bool kPair = false>
 __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
   using L = BwdSmem<D>;
   using R = BwdRoles<kMod || D == 64>;
+  static_assert(!kPair || D == 128, "CTA pairs split 128 head-dim rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -246,7 +258,9 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarKVEmpty), 3);  // every issuer commits
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      mbar_init(bar(L::kBarQEmpty + s), 1);
+      // with pairs the stage also receives the partner's dQ^T rows: its 64
+      // keeping threads hand it back
+      mbar_init(bar(L::kBarQEmpty + s), kPair ? 64 : 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
     for (int s = 0; s < 2; ++s) {
@@ -260,6 +274,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarDKVEmpty), 128);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFree + s), 1);
     for (int s = 0; s < 3; ++s) mbar_init(bar(L::kBarDrain + s), 1);
+    mbar_init(bar(L::kBarPeerReady), 1);
+    mbar_init(bar(L::kBarRecvFull), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -274,7 +290,12 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     tma_prefetch_desc(&tm_do);
   }
   tc_fence_before();
-  __syncthreads();
+  // with pairs, the partner's barriers must be initialised before either CTA
+  // signals the other
+  if (kPair)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after();
   // the prologue above overlaps the preprocess kernel; its outputs (LSE2,
   // Delta, the cleared dQ accumulator and semaphores) are read from here on
@@ -282,6 +303,12 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
   grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  // the units this CTA walks: its own, or its pair's with tile 2p + rank
+  auto next_unit = [&](int r) { return bwd_cta_unit_p<kPair>(a, r); };
+  auto unit_of = [&](int u) {
+    return kPair ? bwd_unit_pair<kMod, kQB>(a, u, group, (int)rank) : bwd_unit<kMod, kQB>(a, u, group);
+  };
 
   if (warp == R::kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -301,8 +328,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         }
         return true;
       };
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
+      for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+        const BwdUnit w = unit_of(u);
         // The unit's first block's Q / dO go out before its K / V: its stage
         // frees up while the previous unit still holds K and V, so it has landed
         // by the time K and V can be replaced.  Later blocks follow K and V, which
@@ -353,8 +380,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       const int role = warp - R::kScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-        const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
+      for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+        const BwdUnit w = unit_of(u);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (role < 2) {
@@ -449,7 +476,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
             // S^T, dP^T (done before the softmax warps published P^T / dS^T),
             // dV and dK of this block are complete: the stage and the S^T buffer
             // can be reused
-            umma_commit(bar(L::kBarQEmpty + it % L::kStages));
+            // (with pairs the drain hands the stage back after the exchange)
+            if (!kPair) umma_commit(bar(L::kBarQEmpty + it % L::kStages));
             umma_commit(bar(L::kBarSFree + (it & 1)));
             // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
             // previous block has emptied the dQ^T columns
@@ -489,8 +517,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     uint8_t* ds_rows = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
     bool ok = true;
-    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
-      const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
+    for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri)) {
+      const BwdUnit w = unit_of(u);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= w.kv_len;
       for (int t = 0; t < w.n_it; ++t, ++it) {
@@ -596,8 +624,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
-    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
-      const BwdUnit w = bwd_unit<kMod, kQB>(a, u, group);
+    for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+      const BwdUnit w = unit_of(u);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
@@ -610,7 +638,61 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         // 32 consecutive floats, one 128-byte line per instruction.
         constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
-        if (!a.deterministic) {
+        if (kPair) {
+          // This CTA keeps head-dim rows [64 rank, 64 rank + 64) of the pair's
+          // dQ^T and sends the partner the other 64.  Both halves of the row
+          // come out of TMEM first (64 values), and the columns go back.
+          uint32_t v0[32], v1[32];
+          tmem_ld32(t_row + L::kColDQ, v0);
+          tmem_ld32(t_row + L::kColDQ + 32, v1);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDQEmpty));
+          // dQ^T(i) completing implies that every MMA reading this block's
+          // stage has completed, and the softmax warps read its LSE2 / Delta
+          // before publishing dS^T: the stage's Q area (16 KB) receives the
+          // partner's 64 rows, laid out [query][row] (256 bytes per query)
+          const uint32_t peer = rank ^ 1u;
+          const uint32_t recv = sbase + stage_off(it);
+          if (r == 0) {
+            mbar_arrive_expect_tx(bar(L::kBarRecvFull), 64 * kQB * 4);
+            mbar_arrive_remote(map_peer(bar(L::kBarPeerReady), peer));
+          }
+          const int rr = r & 63;
+          if ((uint32_t)(r >> 6) != rank) {
+            // sender: once the partner's stage is free, 64 four-byte stores into
+            // it; for each query the 32 lanes write one 128-byte row piece
+            good = __all_sync(0xffffffffu,
+                              mbar_wait_cluster(bar(L::kBarPeerReady), it & 1, abort_flag));
+            if (good) {
+              const uint32_t dst = map_peer(recv, peer) + rr * 4;
+              const uint32_t rbar = map_peer(bar(L::kBarRecvFull), peer);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) st_async_b32(dst + e * 256, v0[e], rbar);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) st_async_b32(dst + (32 + e) * 256, v1[e], rbar);
+            }
+          } else {
+            // keeper: the partner's rows have landed; add rank 0's partial plus
+            // rank 1's, in that order, into the accumulator, then hand the stage
+            // back to the producer
+            good = __all_sync(0xffffffffu,
+                              mbar_wait_cluster(bar(L::kBarRecvFull), it & 1, abort_flag));
+            if (good) {
+              const float* in = reinterpret_cast<const float*>(smem + stage_off(it)) + rr;
+              float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
+#pragma unroll
+              for (int e = 0; e < 64; ++e) {
+                const float own = u2f(e < 32 ? v0[e] : v1[e - 32]);
+                const float other = in[e * 64];
+                const float x = rank == 0 ? own + other : other + own;
+                asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
+                             "f"(x)
+                             : "memory");
+              }
+            }
+            mbar_arrive(bar(L::kBarQEmpty + it % L::kStages));
+          }
+        } else if (!a.deterministic) {
           // two 32-column halves, so that only 32 values are live at a time;
           // the columns are released once the second half is read
           float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
@@ -752,7 +834,12 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // with pairs, neither CTA leaves while its partner may still write into its
+  // shared memory
+  if (kPair)
+    cluster_sync_all();
+  else
+    __syncthreads();
   if (warp == R::kScoreWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
@@ -801,6 +888,57 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
   }
 }
 
+// CTA pairs are built but not dispatched: measured slower (see the kernel's
+// comment on kPair).
+constexpr bool kUsePairs = false;
+
+// The atomic-mode D = 128 main kernel in clusters of two CTAs: the units are
+// pairs of kv tiles, and the grid is as many clusters as can be resident at
+// once (up to one per pair unit), two CTAs each.
+static int launch_bwd_pairs(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, bool mod,
+                            cudaStream_t stream) {
+  using L = BwdSmem<128>;
+  constexpr int kThreads = BwdRoles<false>::kThreads;
+  const auto kernel = mod ? bwd_main<128, true, true> : bwd_main<128, false, true>;
+  const int threads = mod ? BwdRoles<true>::kThreads : kThreads;
+  int dev;
+  DeviceInfo info;
+  if (!current_device(&dev, &info) || dev >= 64) return FA_ERR_CUDA;
+  static int max_clusters[64][2] = {};
+  int& mc = max_clusters[dev][mod ? 1 : 0];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = L::kAllocBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  if (mc == 0) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAllocBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    cfg.gridDim = dim3(info.sm_count & ~1);
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kernel, &cfg) != cudaSuccess || n < 1)
+      return FA_ERR_CUDA;
+    mc = n;
+  }
+  BwdArgs ap = a;
+  ap.n_units = a.B * a.Hkv * ((a.n_ktiles + 1) / 2);
+  const int clusters = ap.n_units < mc ? ap.n_units : mc;
+  cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1));
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, ap) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 template <int D>
 static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
@@ -843,6 +981,11 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (a.qblk_rows == 128) {
       const int rc = launch_bwd_main_q128(tq, tk, tv, tdo, a, mod, grid, stream);
       if (rc != FA_OK) return rc;
+    } else if (D == 128 && !a.deterministic && kUsePairs) {
+      if constexpr (D == 128) {
+        const int rc = launch_bwd_pairs(tq, tk, tv, tdo, a, mod, stream);
+        if (rc != FA_OK) return rc;
+      }
     } else if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);

@@ -78,10 +78,7 @@ struct FwdLayout {
 // the CTA walks the same sequence.
 __device__ __forceinline__ int cta_unit(const FwdArgs& a, int r) {
   int k;
-  if (a.sched == 1) {
-    if (r >= a.chunk) return -1;
-    k = blockIdx.x * a.chunk + r;
-  } else if (a.sched == 2) {
+  if (a.sched == 2) {
     // boustrophedon: each round of gridDim.x units alternates direction, so
     // CTAs that got a longer unit in one round get a shorter one in the next
     k = r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
@@ -92,11 +89,10 @@ __device__ __forceinline__ int cta_unit(const FwdArgs& a, int r) {
 }
 
 // Unit u -> (flat batch*head index, tile pair p: query tiles 2p and 2p+1).
-//   sched 0 / 1: head-major, so CTAs running at the same time share the K/V of
-//                few heads in L2; causal pairs alternate longest / shortest
-//                inside a head so contiguous chunks carry near-equal work.
+//   sched 0:     head-major (non-causal, and windows), so CTAs running at the
+//                same time share the K/V of few heads in L2.
 //   sched 2:     longest pairs of every head first (causal work grows with the
-//                pair index), used when all K/V fit in L2.
+//                pair index), dealt in a snake.
 //   sched 3:     split-KV; the pairs of one (head, split) are adjacent, so
 //                they run together and share that split's K/V in L2.
 __device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, int& pair,
@@ -117,8 +113,7 @@ __device__ __forceinline__ void unit_coords(const FwdArgs& a, int u, int& bh, in
     return;
   }
   bh = u / np;
-  const int r = u - bh * np;
-  pair = a.causal ? ((r & 1) ? (r >> 1) : (np - 1 - (r >> 1))) : r;
+  pair = u - bh * np;
 }
 
 // Keys of batch b that exist: seqlens_k[b] clamped to [0, Sk] (the key padding
@@ -760,24 +755,19 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   a.status = status;
   const int sms = info.sm_count;
   int grid;
-  const double kv_bytes = 2.0 * a.B * a.Hkv * (double)a.Sk * D * 2;
   if (a.n_split > 1) {
     a.sched = 3;
     a.chunk = 0;
     grid = a.n_units < sms ? a.n_units : sms;
-  } else if (a.causal && kv_bytes <= 64.0 * (1 << 20)) {
-    // all K/V fit comfortably in L2: longest-first snake over every head
+  } else if (a.causal) {
+    // longest-first snake over every head.  Also when K/V exceed L2: the CTAs
+    // working on one head's pairs at the same time stream its K/V together
+    // (measured on GB300 against contiguous per-CTA chunks of a head's pairs:
+    // B2 H16 S8192 1,092 -> 1,267 TFLOP/s, S=16k 1,162 -> 1,350, S=32k
+    // 1,369 -> 1,418; the chunks also left 24 SMs idle)
     a.sched = 2;
     a.chunk = 0;
     grid = a.n_units < sms ? a.n_units : sms;
-  } else if (a.causal) {
-    // contiguous chunks of an even number of units: a long and a short tile pair
-    // of the same head come together, so chunks carry near-equal work
-    int chunk = (a.n_units + sms - 1) / sms;
-    if (chunk > 1 && (chunk & 1)) ++chunk;
-    a.sched = 1;
-    a.chunk = chunk;
-    grid = (a.n_units + chunk - 1) / chunk;
   } else {
     a.sched = 0;
     a.chunk = 0;

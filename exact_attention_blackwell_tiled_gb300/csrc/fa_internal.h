@@ -46,10 +46,10 @@ struct FwdArgs {
   int n_qtiles;
   int n_pairs;  // pairs of 128-row query tiles, the forward's unit of work
   int n_units;
-  int sched;  // 0: round robin over head-major units; 1: contiguous chunks of
-              // `chunk` units; 2: longest-first snake over all heads; 3: split-KV,
-              // units (head, split, pair) round robin
-  int chunk;
+  int sched;  // 0: round robin over head-major units; 2: longest-first snake
+              // over all heads (causal); 3: split-KV, units (head, split, pair)
+              // round robin
+  int chunk;  // unused (0)
   // split-KV: split s holds kv tiles [s * split_tiles, (s + 1) * split_tiles);
   // each (query tile, split) writes its own normalised O and LSE to the parts
   int n_split;

@@ -133,22 +133,21 @@ def _kv_bytes(w: synth.Workload) -> int:
 
 
 @pytest.mark.parametrize("S", [1024, 2048, 32768])
-def test_sweep_causal_d128_chunked(S):
-    """Causal D=128 sweep points.  Their K/V exceed 64 MiB, so the forward deals
-    each CTA a contiguous chunk of head-major units, a long and a short tile
-    pair of a head together (the chunked causal schedule); at S=32768 the 2048
-    units make 146 chunks of 14 and a last chunk of 4.  Sampled rows of every
-    head and two whole heads against the oracle."""
+def test_sweep_causal_d128_large_kv(S):
+    """Causal D=128 sweep points, whose K/V exceed L2 (128 MiB at S <= 16k,
+    256 MiB at 32k): the longest-first snake deals every head's tile pairs to
+    all SMs at once.  At S=32768 the 2048 units take 14 rounds of 152 CTAs with
+    a partial last round.  Sampled rows of every head and two whole heads
+    against the oracle."""
     w = synth.sweep(S, 128, True)
-    assert _kv_bytes(w) > 64 << 20, "this shape no longer takes the chunked schedule"
+    assert _kv_bytes(w) > 64 << 20
     _sampled(w, 32, 2)
 
 
 def test_bwd_workload_forward_sampled():
     """The forward of the backward workload (B=2, H=16, S=8192, D=128, causal),
-    which gives the backward its O and LSE: K/V of 128 MiB, the chunked causal
-    schedule.  O and LSE checked on sampled rows of every head and two whole
-    heads."""
+    which gives the backward its O and LSE (K/V of 128 MiB).  O and LSE checked
+    on sampled rows of every head and two whole heads."""
     w = synth.BWD
     assert _kv_bytes(w) > 64 << 20
     _sampled(w, 32, 2)
