@@ -298,9 +298,12 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrives once on the mbarrier at shared::cluster address `remote_bar`.
+// Arrives once on the mbarrier at shared::cluster address `remote_bar`, with
+// relaxed ordering: the arrival publishes no data of this thread (a release
+// would first wait for every earlier global write of the thread, measured at
+// about 1,000 cycles behind the drain's reduction adds).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
 
@@ -313,11 +316,14 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, u
       : "memory");
 }
 
+// Non-blocking test (test_wait, not try_wait: a try_wait may sleep for a
+// system-dependent time, which measured about 1,000 cycles before it saw an
+// arrival made by the other CTA of the pair).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)

@@ -211,7 +211,7 @@ struct BwdSmem {
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
   static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
   // CTA pairs (atomic dQ at D = 128): the partner's stage is free to receive
-  // (arrived by the partner), and the partner's dQ^T rows have arrived (tx)
+  // (arrived by the partner), and the partner's dQ^T partial has arrived (tx)
   static constexpr int kBarPeerReady = kBarDrain + 3;
   static constexpr int kBarRecvFull = kBarPeerReady + 1;
   static constexpr int kNumBars = kBarRecvFull + 1;
@@ -224,14 +224,15 @@ struct BwdSmem {
 };
 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
-// plain kernel applies no mask or the causal one.  kPair (atomic dQ, D = 128):
-// clusters of two CTAs take adjacent kv tiles 2p, 2p+1 of one head and walk
-// the same query blocks; per block each CTA keeps 64 head-dim rows of dQ^T,
-// receives the partner's partial of those rows into the block's stage (whose
-// Q / dO the MMAs have finished with) through distributed shared memory,
-// and adds the sum: the pair reduces over 256 keys before the global adds,
-// which halves the fp32 reduction traffic into L2 (FlashAttention-4 pages,
-// key contribution #3: a restructured dQ reduction with half the atomic adds).
+// plain kernel applies no mask or the causal one.  kPair (atomic dQ, D = 128,
+// plain): clusters of two CTAs take adjacent kv tiles 2p, 2p+1 of one head and
+// walk the same query blocks; per block each CTA keeps the dQ^T partial of its
+// rank's 32 queries, receives the partner's partial of those queries into the
+// block's stage (whose Q / dO the MMAs have finished with) through distributed
+// shared memory, and adds the sum: the pair reduces over 256 keys before the
+// global adds, which halves the fp32 reduction traffic into L2
+// (FlashAttention-4 pages, key contribution #3: a restructured dQ reduction
+// with half the atomic adds).
 template <int D, bool kMod, bool kPair = false>
 __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -258,9 +259,9 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarKVEmpty), 3);  // every issuer commits
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      // with pairs the stage also receives the partner's dQ^T rows: its 64
-      // keeping threads hand it back
-      mbar_init(bar(L::kBarQEmpty + s), kPair ? 64 : 1);
+      // with pairs the stage also receives the partner's dQ^T partial: the
+      // 128 drain threads hand it back
+      mbar_init(bar(L::kBarQEmpty + s), kPair ? 128 : 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
     for (int s = 0; s < 2; ++s) {
@@ -639,9 +640,10 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
         if (kPair) {
-          // This CTA keeps head-dim rows [64 rank, 64 rank + 64) of the pair's
-          // dQ^T and sends the partner the other 64.  Both halves of the row
-          // come out of TMEM first (64 values), and the columns go back.
+          // This CTA keeps queries [32 rank, 32 rank + 32) of the block and
+          // sends its partner its partial for the other 32: each of the 128
+          // threads (head-dim row r) sends 32 values and adds 32.  Both halves of
+          // the row come out of TMEM first, and the columns go back.
           uint32_t v0[32], v1[32];
           tmem_ld32(t_row + L::kColDQ, v0);
           tmem_ld32(t_row + L::kColDQ + 32, v1);
@@ -650,48 +652,51 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           // dQ^T(i) completing implies that every MMA reading this block's
           // stage has completed, and the softmax warps read its LSE2 / Delta
           // before publishing dS^T: the stage's Q area (16 KB) receives the
-          // partner's 64 rows, laid out [query][row] (256 bytes per query)
+          // partner's partial of this CTA's 32 queries, laid out [query][row]
+          // (512 bytes per query)
           const uint32_t peer = rank ^ 1u;
-          const uint32_t recv = sbase + stage_off(it);
           if (r == 0) {
-            mbar_arrive_expect_tx(bar(L::kBarRecvFull), 64 * kQB * 4);
+            mbar_arrive_expect_tx(bar(L::kBarRecvFull), 32 * D * 4);
             mbar_arrive_remote(map_peer(bar(L::kBarPeerReady), peer));
           }
-          const int rr = r & 63;
-          if ((uint32_t)(r >> 6) != rank) {
-            // sender: once the partner's stage is free, 64 four-byte stores into
-            // it; for each query the 32 lanes write one 128-byte row piece
-            good = __all_sync(0xffffffffu,
-                              mbar_wait_cluster(bar(L::kBarPeerReady), it & 1, abort_flag));
-            if (good) {
-              const uint32_t dst = map_peer(recv, peer) + rr * 4;
-              const uint32_t rbar = map_peer(bar(L::kBarRecvFull), peer);
+          // send: once the partner's stage is free, 32 four-byte stores into it;
+          // for each query the 32 lanes write one 128-byte row piece
+          good = __all_sync(0xffffffffu,
+                            mbar_wait_cluster(bar(L::kBarPeerReady), it & 1, abort_flag));
+          if (good) {
+            const uint32_t dst = map_peer(sbase + stage_off(it), peer) + r * 4;
+            const uint32_t rbar = map_peer(bar(L::kBarRecvFull), peer);
+            // the partner keeps queries [32 peer, +32): v0 for rank 0, v1 for rank 1
 #pragma unroll
-              for (int e = 0; e < 32; ++e) st_async_b32(dst + e * 256, v0[e], rbar);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) st_async_b32(dst + (32 + e) * 256, v1[e], rbar);
-            }
-          } else {
-            // keeper: the partner's rows have landed; add rank 0's partial plus
-            // rank 1's, in that order, into the accumulator, then hand the stage
-            // back to the producer
+            for (int e = 0; e < 32; ++e)
+              st_async_b32(dst + e * (D * 4), peer == 0 ? v0[e] : v1[e], rbar);
+          }
+          // keep: the partner's partial of this CTA's queries has landed; add
+          // rank 0's partial plus rank 1's, in that order, then hand the stage
+          // back to the producer
+          if (good)
             good = __all_sync(0xffffffffu,
                               mbar_wait_cluster(bar(L::kBarRecvFull), it & 1, abort_flag));
-            if (good) {
-              const float* in = reinterpret_cast<const float*>(smem + stage_off(it)) + rr;
-              float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
+          if (good) {
+            // all 32 received values first: each add below is an asm statement
+            // with a memory clobber, which would otherwise order every
+            // shared-memory load after the previous add
+            const float* in = reinterpret_cast<const float*>(smem + stage_off(it)) + r;
+            float other[32];
 #pragma unroll
-              for (int e = 0; e < 64; ++e) {
-                const float own = u2f(e < 32 ? v0[e] : v1[e - 32]);
-                const float other = in[e * 64];
-                const float x = rank == 0 ? own + other : other + own;
-                asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
-                             "f"(x)
-                             : "memory");
-              }
+            for (int e = 0; e < 32; ++e) other[e] = in[e * D];
+            float* dst = a.dq_acc +
+                         ((size_t)bh * a.Sq_pad + (size_t)iq * kQB + 32 * rank) * D + r;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float own = u2f(rank == 0 ? v0[e] : v1[e]);
+              const float x = rank == 0 ? own + other[e] : other[e] + own;
+              asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
+                           "f"(x)
+                           : "memory");
             }
-            mbar_arrive(bar(L::kBarQEmpty + it % L::kStages));
           }
+          mbar_arrive(bar(L::kBarQEmpty + it % L::kStages));
         } else if (!a.deterministic) {
           // two 32-column halves, so that only 32 values are live at a time;
           // the columns are released once the second half is read
@@ -888,8 +893,9 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
   }
 }
 
-// CTA pairs are built but not dispatched: measured slower (see the kernel's
-// comment on kPair).
+// CTA pairs are built but not dispatched: measured slower at B2 H16 S8192
+// causal (868 against 1,184 TFLOP/s), the exchange making each block's drain
+// longer than the block period.
 constexpr bool kUsePairs = false;
 
 // The atomic-mode D = 128 main kernel in clusters of two CTAs: the units are
@@ -981,7 +987,7 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (a.qblk_rows == 128) {
       const int rc = launch_bwd_main_q128(tq, tk, tv, tdo, a, mod, grid, stream);
       if (rc != FA_OK) return rc;
-    } else if (D == 128 && !a.deterministic && kUsePairs) {
+    } else if (D == 128 && !a.deterministic && kUsePairs && !mod) {
       if constexpr (D == 128) {
         const int rc = launch_bwd_pairs(tq, tk, tv, tdo, a, mod, stream);
         if (rc != FA_OK) return rc;
