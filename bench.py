@@ -13,7 +13,8 @@ Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   torchrun --nproc-per-node N bench.py --gpus N ...   (one rank per GPU)
   python bench.py --only fwd:S:D:causal --steps K --warmup W
-      (one forward shape alone, for a profiler capture of that kernel)
+  python bench.py --only bwd:S:D:causal[:det] --steps K --warmup W
+      (one forward or backward shape alone, for a profiler capture)
 
 With N > 1 every rank runs its own batch of the same workload (independent
 units, no collective on the data path); the timing is the max over ranks and
@@ -490,32 +491,49 @@ def run_ours(args):
 
 
 def run_only(fa, args, dev):
-    """One forward shape alone (``--only fwd:S:D:causal``): W + K launches of the
-    forward kernel on the sweep workload of that S and D, nothing else -- the
-    command a profiler capture of that kernel runs."""
+    """One kernel call shape alone, W + K times, nothing else -- the command a
+    profiler capture of that kernel runs:
+      --only fwd:S:D:causal        the forward on the sweep workload of that S, D
+      --only bwd:S:D:causal[:det]  the backward (atomic or deterministic dQ) on it
+    """
     import torch
-    kind, S, D, c = args.only.split(":")
-    if kind != "fwd":
+    parts = args.only.split(":")
+    kind, S, D, c = parts[:4]
+    det = len(parts) > 4 and parts[4] == "det"
+    if kind not in ("fwd", "bwd"):
         raise SystemExit(f"--only: unknown kind {kind!r}")
     w = synth.sweep(int(S), int(D), c in ("1", "c", "causal", "true"))
     gen = torch.Generator(device=dev).manual_seed(w.seed)
-    q, k, v = (torch.randn(w.B, w.Hq, w.Sq, w.D, device=dev, generator=gen).to(torch.bfloat16)
-               for _ in range(3))
+    q, k, v, do = (torch.randn(w.B, w.Hq, w.Sq, w.D, device=dev, generator=gen).to(torch.bfloat16)
+                   for _ in range(4))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    ws = grads = None
+    if kind == "bwd":
+        ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det),
+                         dtype=torch.uint8, device=dev)
+        grads = [torch.empty_like(q) for _ in range(3)]
     ev = []
     for i in range(args.warmup + args.steps):
         e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         fa.set_timing_events(*e)
-        fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+        if kind == "fwd":
+            fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+        else:
+            fa.bwd(q, k, v, o, do, lse, causal=w.causal, workspace=ws, dq=grads[0], dk=grads[1],
+                   dv=grads[2], deterministic=det)
         if i >= args.warmup:
             ev.append(e)
     torch.cuda.synchronize(dev)
     assert fa.fwd_status() == fa.FA_OK
+    if ws is not None:
+        assert fa.bwd_status(ws) == fa.FA_OK
     ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+    flops = w.flops(backward=(kind == "bwd"))
     print(json.dumps({"only": args.only, "workload": w.name, "B": w.B, "H": w.Hq, "S": w.Sq,
-                      "D": w.D, "causal": w.causal, "ms": round(ms, 4),
-                      "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1)}), flush=True)
+                      "D": w.D, "causal": w.causal, "deterministic": det, "ms": round(ms, 4),
+                      "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}), flush=True)
 
 
 def fwd_sweep(fa, dev, peak, iters=10, shapes=None):
@@ -755,7 +773,8 @@ def main(argv=None):
     ap.add_argument("--no-long-fwd", action="store_true",
                     help="skip the non-causal S >= 8k forward reported under extra")
     ap.add_argument("--only", default=None,
-                    help="fwd:S:D:causal -- time one forward shape alone and exit")
+                    help="fwd:S:D:causal or bwd:S:D:causal[:det] -- time one kernel call "
+                         "shape alone and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
