@@ -112,12 +112,21 @@ struct BwdArgs {
                            // semaphore i of a head counts the writers of block i
 };
 
-constexpr int kDetGroups = 4;  // deterministic-mode accumulators (at most)
+constexpr int kDetGroups = 4;       // deterministic-mode accumulators (at most)
+constexpr int kDetGroupsLong = 2;   // ... from kDetLongTiles kv tiles on
+constexpr int kDetLongTiles = 32;
 
-// Accumulators of a backward call: 1 atomic, else min(kDetGroups, kv tiles).
+// Accumulators of a backward call: 1 atomic, else min(G, kv tiles) with G = 4,
+// or 2 from 32 kv tiles on.  Measured on GB300 (main kernel + the convert that
+// sums the accumulators): at B2 H16 S8192 (64 kv tiles) 1 / 2 / 4 / 8 groups
+// took 1.95 / 1.92 / 2.08 / 1.94 ms of main kernel, the convert growing with
+// the count; at B4 H16 S2048 (16 tiles) 0.31 / 0.30 / 0.26 / 0.24 ms, where 4
+// gives the shortest total.
 inline int dq_group_count(int Sk, int deterministic) {
   const int n_ktiles = (Sk + kTile - 1) / kTile;
-  return deterministic ? (n_ktiles < kDetGroups ? (n_ktiles > 0 ? n_ktiles : 1) : kDetGroups) : 1;
+  if (!deterministic) return 1;
+  const int g = n_ktiles >= kDetLongTiles ? kDetGroupsLong : kDetGroups;
+  return n_ktiles < g ? (n_ktiles > 0 ? n_ktiles : 1) : g;
 }
 
 struct BwdLayout {

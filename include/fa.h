@@ -115,11 +115,12 @@ int fa_fwd_status(fa_stream_t stream);
 /*
  * Bytes of device workspace fa_bwd needs for these sizes (0 on bad sizes).  The
  * workspace holds fp32 dQ accumulators [B, Hq, ceil(Sq/128)*128, D] (one in the
- * atomic mode; in the deterministic mode min(4, ceil(Sk/128)), kv tile j adding
- * into accumulator j % 4 in its own ordered chain, the accumulators summed in
- * fixed order at the end), the per-row dot products D_i = dO_i . O_i and
+ * atomic mode; in the deterministic mode G = min(4, ceil(Sk/128)), or
+ * min(2, ceil(Sk/128)) from 32 kv tiles (Sk > 3968) on, kv tile j adding into
+ * accumulator j % G in its own ordered chain, the accumulators summed in fixed
+ * order at the end), the per-row dot products D_i = dO_i . O_i and
  * LSE*log2(e) (fp32 [B, Hq, padded Sq]), the deterministic mode's per-(group,
- * b, h, 64-row query block) semaphores and a status word.  The deterministic
+ * b, h, query block) semaphores and a status word.  The deterministic
  * size is at least the atomic one.  It needs no initialisation: fa_bwd clears
  * or overwrites what it uses.
  */
@@ -277,7 +278,8 @@ int fa_set_timing_events(void* start_event, void* stop_event);
  *   - Sizes whose workspace (fa_bwd_workspace_bytes) exceeds 32 MiB are
  *     rejected with FA_ERR_WORKSPACE (about 64,000 query rows B*Hq*Sq at
  *     D = 128, about 127,000 at D = 64; in the deterministic mode, which keeps up
- *     to four accumulators, about a quarter of those); invalid sizes return
+ *     to four accumulators (two from 32 kv tiles on), about a quarter or a half
+ *     of those); invalid sizes return
  *     FA_ERR_INVALID_ARG.
  *   - The first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
