@@ -463,10 +463,12 @@ __global__ void __launch_bounds__(320, 1)
         };
         if (c > 0.f) {
           // Common case.  Pass 1: the whole score row in one TMEM round trip,
-          // reduced to its max (masked columns skipped).
+          // reduced to its max (masked columns skipped).  The plain kernel keeps
+          // the row in registers for pass 2; the score-modified kernels, which
+          // carry more live state, reload it.
           float mraw = -INFINITY;
+          uint32_t v[kTile];
           {
-            uint32_t v[kTile];
             tmem_ld128(t_row + col_s, v);
             if (masked_tile) {
 #pragma unroll
@@ -501,14 +503,22 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t w0[32], w1[32], pk[32];
-            __syncwarp();
-            tmem_ld32(t_row + col_s + h * 64, w0);
-            tmem_ld32(t_row + col_s + h * 64 + 32, w1);
-            if (masked_tile) {
+            if constexpr (kMod == 0) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                if (hidden(kv0 + h * 64 + i)) w0[i] = __float_as_uint(-INFINITY);
-                if (hidden(kv0 + h * 64 + 32 + i)) w1[i] = __float_as_uint(-INFINITY);
+                w0[i] = v[h * 64 + i];
+                w1[i] = v[h * 64 + 32 + i];
+              }
+            } else {
+              __syncwarp();
+              tmem_ld32(t_row + col_s + h * 64, w0);
+              tmem_ld32(t_row + col_s + h * 64 + 32, w1);
+              if (masked_tile) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  if (hidden(kv0 + h * 64 + i)) w0[i] = __float_as_uint(-INFINITY);
+                  if (hidden(kv0 + h * 64 + 32 + i)) w1[i] = __float_as_uint(-INFINITY);
+                }
               }
             }
 #pragma unroll
