@@ -157,7 +157,6 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
   }
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]);
 
 // Writes n consecutive 32-bit columns of this thread's lane (no wait).
 template <int N>
@@ -174,15 +173,6 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&w)[N]) 
   }
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
-      "r"(w[15])
-      : "memory");
-}
 
 // Iterations (q head of the group x query block) of kv tile j.
 struct BwdUnit {

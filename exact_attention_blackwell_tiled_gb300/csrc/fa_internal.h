@@ -61,6 +61,7 @@ struct FwdArgs {
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdArgs& a, int D, cudaStream_t stream);
 
+
 // Log-sum-exp merge of n attention parts over disjoint key sets.
 struct MergeArgs {
   const float* o_part;    // [n, rows, D] fp32, normalised per part
