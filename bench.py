@@ -294,9 +294,28 @@ def time_step(fa, w, dev, tensors, steps, warmup, flush, world, stream):
     assert fa.bwd_status(ws_det) == fa.FA_OK
     det_ms = [a.elapsed_time(b) for a, b in det]
     del ws_det
+    # the CTA-pair main kernel (2-CTA MMA, dQ reduced over 256 keys), where it applies
+    pair = []
+    if w.D == 128:
+        prev = fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR)
+        try:
+            for i in range(min(steps, 50) + 3):
+                flush.zero_()
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                fa.set_timing_events(*e)
+                fa.bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=scale, workspace=ws,
+                       dq=dq, dk=dk, dv=dv)
+                if i >= 3:
+                    pair.append(e)
+            torch.cuda.synchronize(dev)
+        finally:
+            fa.set_bwd_kernel(prev)
+        assert fa.bwd_status(ws) == fa.FA_OK
+    pair_ms = [a.elapsed_time(b) for a, b in pair]
     return {"step_ms": step_ms, "launches": launches, "clocks": clk.summary(),
             "fwd_ms": sum(fwd_ms) / len(fwd_ms), "bwd_main_ms": sum(bwd_main_ms) / len(bwd_main_ms),
-            "det_ms": sum(det_ms) / len(det_ms)}
+            "det_ms": sum(det_ms) / len(det_ms),
+            "pair_ms": sum(pair_ms) / len(pair_ms) if pair_ms else None}
 
 
 def kernel_rates(w, t, peak):
@@ -314,6 +333,8 @@ def kernel_rates(w, t, peak):
             "bwd_main_frac_of_peak": round(bwd_tf / peak, 4),
             "bwd_main_det_tflops": round(det_tf, 1), "bwd_main_det_ms": round(t["det_ms"], 4),
             "det_over_atomic": round(t["bwd_main_ms"] / t["det_ms"], 3),
+            "bwd_main_pair_tflops": (round(bwd_f / (t["pair_ms"] * 1e-3) / 1e12, 1)
+                                     if t.get("pair_ms") else None),
             "fwd_frac_of_nominal": round(fwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4),
             "bwd_main_frac_of_nominal": round(bwd_tf / NOMINAL_DENSE_BF16_TFLOPS, 4)}
 

@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
 #: every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_status", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_status",
            "fa_status_string", "fa_exp2_test", "fa_last_launch_count", "fa_set_timing_events",
+           "fa_set_bwd_kernel",
            "fa_bwd_noalloc", "fa_fwd_mod", "fa_bwd_mod", "fa_fwd_split_count",
            "fa_fwd_split_workspace_bytes", "fa_fwd_split", "fa_lse_merge", "fa_wait_test",
            "fa_bwd_noalloc_status")
@@ -70,6 +71,8 @@ def _bind(lib):
     lib.fa_last_launch_count.restype = i
     lib.fa_set_timing_events.argtypes = [vp, vp]
     lib.fa_set_timing_events.restype = i
+    lib.fa_set_bwd_kernel.argtypes = [i, vp]
+    lib.fa_set_bwd_kernel.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i,
                                    vp]
     lib.fa_bwd_noalloc.restype = i
@@ -325,6 +328,20 @@ def set_timing_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event 
     rc = lib().fa_set_timing_events(ps, pe)
     if rc != FA_OK:
         raise FAError("fa_set_timing_events", rc)
+
+
+BWD_KERNEL_AUTO, BWD_KERNEL_ONE_SM, BWD_KERNEL_PAIR = 0, 1, 2
+
+
+def set_bwd_kernel(kind: int) -> int:
+    """Backward main kernel for head dim 128, atomic dQ, no score modification
+    (fa_set_bwd_kernel): BWD_KERNEL_AUTO, BWD_KERNEL_ONE_SM or BWD_KERNEL_PAIR
+    (CTA pairs, 2-CTA MMA).  Returns the previous setting."""
+    prev = ctypes.c_int(0)
+    rc = lib().fa_set_bwd_kernel(int(kind), ctypes.byref(prev))
+    if rc != FA_OK:
+        raise FAError("fa_set_bwd_kernel", rc)
+    return prev.value
 
 
 class _Attention(torch.autograd.Function):

@@ -1,7 +1,8 @@
 // bwd_common.cuh -- device helpers shared by the backward main kernels
-// (64-row and 128-row query blocks): the visibility window, the kv tile ->
-// query block ranges and the deterministic chain's contributors, the unit
-// schedule, bounded waits and the TMEM load / store shapes they use.
+// (64-row and 128-row query blocks, CTA pairs): the visibility window, the kv
+// tile -> query block ranges and the deterministic chain's contributors, the
+// unit schedule, bounded waits, the TMEM load / store shapes they use, and the
+// cluster and 2-CTA (cta_group::2) building blocks of the pair kernel.
 #pragma once
 
 #include <climits>
@@ -196,11 +197,9 @@ __device__ __forceinline__ int bwd_cta_unit(const BwdArgs& a, int r) {
   return k < a.n_units ? k : -1;
 }
 
-// The same dealing over clusters of two CTAs (kPair): both CTAs of cluster c =
-// blockIdx.x / 2 walk the same pair units.
-template <bool kPair>
-__device__ __forceinline__ int bwd_cta_unit_p(const BwdArgs& a, int r) {
-  if (!kPair) return bwd_cta_unit(a, r);
+// The same dealing over clusters of two CTAs (the CTA-pair kernel): both CTAs
+// of cluster c = blockIdx.x / 2 walk the same pair units.
+__device__ __forceinline__ int bwd_cta_unit_pair(const BwdArgs& a, int r) {
   const int id = (int)(blockIdx.x >> 1), n = (int)(gridDim.x >> 1);
   const int k = a.snake ? r * n + ((r & 1) ? n - 1 - id : id) : id + r * n;
   return k < a.n_units ? k : -1;
@@ -297,15 +296,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
                : "memory");
 }
 
-// Stores 4 bytes into another CTA's shared memory; the write counts 4 bytes of
-// transaction on the mbarrier at `remote_bar` (same CTA as `remote_addr`).
-__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
-      "r"(v), "r"(remote_bar)
-      : "memory");
-}
-
 // Non-blocking test (test_wait, not try_wait: a try_wait may sleep for a
 // system-dependent time, which measured about 1,000 cycles before it saw an
 // arrival made by the other CTA of the pair).
@@ -337,6 +327,101 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// ------------------------------------------------------------------ CTA pairs (tcgen05 cta_group::2)
+//
+// Two CTAs of a cluster share the tensor cores of their two SMs: one thread of
+// rank 0 issues every MMA, which runs its first M/2 rows on rank 0's SM and
+// the rest on rank 1's; each SM reads the A rows and the B columns of its half
+// from its own shared memory (or TMEM), at the same addresses in both CTAs,
+// and writes its own TMEM.  Every tcgen05 allocation, MMA and commit of such a
+// kernel names the pair.
+
+// One warp of each CTA of the pair allocates (the same count in both).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Pair SS MMA from split descriptors; `acc` selects accumulate (1) or overwrite (0).
+__device__ __forceinline__ void umma_pair_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                             uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Pair TS MMA: A from each CTA's TMEM at `a_tmem`.
+__device__ __forceinline__ void umma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Arrives once on the mbarrier at the same offset in both CTAs when every pair
+// MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_pair_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// ... on this CTA's mbarrier only.
+__device__ __forceinline__ void umma_pair_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 3-D tile load into this CTA's shared memory whose bytes are counted on an
+// mbarrier of either CTA of the pair (`bar`: a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Copies `bytes` (a multiple of 16) of this CTA's shared memory to shared::cluster
+// address `dst` (the partner's) through the async proxy; completion counts the
+// bytes on the mbarrier at `bar`, in the destination CTA.  The source must have
+// been made visible to the async proxy (fence_proxy_async_smem by its writers).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// High word of a shared-memory descriptor with the 64-byte swizzle (layout 4):
+// an MN-major operand whose 64-byte rows hold 32 consecutive MN elements of one
+// K index, 8 K rows (512 bytes) per swizzle atom; SBO = the next 8 K rows.
+__host__ __device__ constexpr uint32_t sdesc_hi_sw64(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
 }
 
 }  // namespace fa

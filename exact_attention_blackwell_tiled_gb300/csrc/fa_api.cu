@@ -181,6 +181,14 @@ const char* fa_status_string(int s) {
 
 int fa_last_launch_count(void) { return t_launches; }
 
+int fa_set_bwd_kernel(int kind, int* previous) {
+  if (kind != FA_BWD_KERNEL_AUTO && kind != FA_BWD_KERNEL_ONE_SM && kind != FA_BWD_KERNEL_PAIR)
+    return FA_ERR_INVALID_ARG;
+  const int was = fa::g_bwd_kernel.exchange(kind);
+  if (previous) *previous = was;
+  return FA_OK;
+}
+
 int fa_set_timing_events(void* start_event, void* stop_event) {
   if ((start_event == nullptr) != (stop_event == nullptr)) return FA_ERR_INVALID_ARG;
   t_ev_start = static_cast<cudaEvent_t>(start_event);
@@ -420,7 +428,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
       workspace_bytes < L.total)
     return FA_ERR_WORKSPACE;
   if ((rc = check_device())) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  BwdMaps maps;
   // Sq == 0 still needs dk = dv = 0: the kernels handle it with zero q tiles.
   // With no q tiles the q / dO maps are never used; they are built over k.
   const void* q_map = has_q ? q : k;
@@ -429,9 +437,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   const int sq_map = has_q ? Sq : Sk;
   // q and dO move in blocks of bwd_qblk_rows rows in the backward pass
   const int qrows = bwd_qblk_rows(D, deterministic);
-  if (!make_tmap_bsd(&tq, q_map, bh_map, sq_map, D, qrows) ||
-      !make_tmap_bsd(&tk, k, B * Hkv, Sk, D) || !make_tmap_bsd(&tv, v, B * Hkv, Sk, D) ||
-      !make_tmap_bsd(&tdo, do_map, bh_map, sq_map, D, qrows))
+  if (!make_tmap_bsd(&maps.q, q_map, bh_map, sq_map, D, qrows) ||
+      !make_tmap_bsd(&maps.k, k, B * Hkv, Sk, D) || !make_tmap_bsd(&maps.v, v, B * Hkv, Sk, D) ||
+      !make_tmap_bsd(&maps.dO, do_map, bh_map, sq_map, D, qrows) ||
+      !make_tmap_bsd(&maps.q_half, q_map, bh_map, sq_map, D, 32) ||
+      !make_tmap_bsd(&maps.dO_half, do_map, bh_map, sq_map, D, 32))
     return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdArgs a{};
@@ -480,7 +490,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.qblk_rows = qrows;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));
+  return launch_bwd(maps, a, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace

@@ -210,11 +210,7 @@ struct BwdSmem {
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
   static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
-  // CTA pairs (atomic dQ at D = 128): the partner's stage is free to receive
-  // (arrived by the partner), and the partner's dQ^T partial has arrived (tx)
-  static constexpr int kBarPeerReady = kBarDrain + 3;
-  static constexpr int kBarRecvFull = kBarPeerReady + 1;
-  static constexpr int kNumBars = kBarRecvFull + 1;
+  static constexpr int kNumBars = kBarDrain + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAllocBytes = kBytes + 1024;
@@ -224,23 +220,14 @@ struct BwdSmem {
 };
 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
-// plain kernel applies no mask or the causal one.  kPair (atomic dQ, D = 128,
-// plain): clusters of two CTAs take adjacent kv tiles 2p, 2p+1 of one head and
-// walk the same query blocks; per block each CTA keeps the dQ^T partial of its
-// rank's 32 queries, receives the partner's partial of those queries into the
-// block's stage (whose Q / dO the MMAs have finished with) through distributed
-// shared memory, and adds the sum: the pair reduces over 256 keys before the
-// global adds, which halves the fp32 reduction traffic into L2
-// (FlashAttention-4 pages, key contribution #3: a restructured dQ reduction
-// with half the atomic adds).
-template <int D, bool kMod, bool kPair = false>
+// plain kernel applies no mask or the causal one.
+template <int D, bool kMod>
 __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
              const BwdArgs a) {
   using L = BwdSmem<D>;
   using R = BwdRoles<kMod || D == 64>;
-  static_assert(!kPair || D == 128, "CTA pairs split 128 head-dim rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -259,9 +246,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarKVEmpty), 3);  // every issuer commits
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      // with pairs the stage also receives the partner's dQ^T partial: the
-      // 128 drain threads hand it back
-      mbar_init(bar(L::kBarQEmpty + s), kPair ? 128 : 1);
+      mbar_init(bar(L::kBarQEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFull + s), 1);
     for (int s = 0; s < 2; ++s) {
@@ -275,8 +260,6 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarDKVEmpty), 128);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFree + s), 1);
     for (int s = 0; s < 3; ++s) mbar_init(bar(L::kBarDrain + s), 1);
-    mbar_init(bar(L::kBarPeerReady), 1);
-    mbar_init(bar(L::kBarRecvFull), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -291,12 +274,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     tma_prefetch_desc(&tm_do);
   }
   tc_fence_before();
-  // with pairs, the partner's barriers must be initialised before either CTA
-  // signals the other
-  if (kPair)
-    cluster_sync_all();
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   // the prologue above overlaps the preprocess kernel; its outputs (LSE2,
   // Delta, the cleared dQ accumulator and semaphores) are read from here on
@@ -304,12 +282,8 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
   grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
-  const uint32_t rank = kPair ? cluster_rank() : 0u;
-  // the units this CTA walks: its own, or its pair's with tile 2p + rank
-  auto next_unit = [&](int r) { return bwd_cta_unit_p<kPair>(a, r); };
-  auto unit_of = [&](int u) {
-    return kPair ? bwd_unit_pair<kMod, kQB>(a, u, group, (int)rank) : bwd_unit<kMod, kQB>(a, u, group);
-  };
+  auto next_unit = [&](int r) { return bwd_cta_unit(a, r); };
+  auto unit_of = [&](int u) { return bwd_unit<kMod, kQB>(a, u, group); };
 
   if (warp == R::kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -477,8 +451,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
             // S^T, dP^T (done before the softmax warps published P^T / dS^T),
             // dV and dK of this block are complete: the stage and the S^T buffer
             // can be reused
-            // (with pairs the drain hands the stage back after the exchange)
-            if (!kPair) umma_commit(bar(L::kBarQEmpty + it % L::kStages));
+            umma_commit(bar(L::kBarQEmpty + it % L::kStages));
             umma_commit(bar(L::kBarSFree + (it & 1)));
             // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
             // previous block has emptied the dQ^T columns
@@ -639,65 +612,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         // 32 consecutive floats, one 128-byte line per instruction.
         constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
-        if (kPair) {
-          // This CTA keeps queries [32 rank, 32 rank + 32) of the block and
-          // sends its partner its partial for the other 32: each of the 128
-          // threads (head-dim row r) sends 32 values and adds 32.  Both halves of
-          // the row come out of TMEM first, and the columns go back.
-          uint32_t v0[32], v1[32];
-          tmem_ld32(t_row + L::kColDQ, v0);
-          tmem_ld32(t_row + L::kColDQ + 32, v1);
-          tc_fence_before();
-          mbar_arrive(bar(L::kBarDQEmpty));
-          // dQ^T(i) completing implies that every MMA reading this block's
-          // stage has completed, and the softmax warps read its LSE2 / Delta
-          // before publishing dS^T: the stage's Q area (16 KB) receives the
-          // partner's partial of this CTA's 32 queries, laid out [query][row]
-          // (512 bytes per query)
-          const uint32_t peer = rank ^ 1u;
-          if (r == 0) {
-            mbar_arrive_expect_tx(bar(L::kBarRecvFull), 32 * D * 4);
-            mbar_arrive_remote(map_peer(bar(L::kBarPeerReady), peer));
-          }
-          // send: once the partner's stage is free, 32 four-byte stores into it;
-          // for each query the 32 lanes write one 128-byte row piece
-          good = __all_sync(0xffffffffu,
-                            mbar_wait_cluster(bar(L::kBarPeerReady), it & 1, abort_flag));
-          if (good) {
-            const uint32_t dst = map_peer(sbase + stage_off(it), peer) + r * 4;
-            const uint32_t rbar = map_peer(bar(L::kBarRecvFull), peer);
-            // the partner keeps queries [32 peer, +32): v0 for rank 0, v1 for rank 1
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              st_async_b32(dst + e * (D * 4), peer == 0 ? v0[e] : v1[e], rbar);
-          }
-          // keep: the partner's partial of this CTA's queries has landed; add
-          // rank 0's partial plus rank 1's, in that order, then hand the stage
-          // back to the producer
-          if (good)
-            good = __all_sync(0xffffffffu,
-                              mbar_wait_cluster(bar(L::kBarRecvFull), it & 1, abort_flag));
-          if (good) {
-            // all 32 received values first: each add below is an asm statement
-            // with a memory clobber, which would otherwise order every
-            // shared-memory load after the previous add
-            const float* in = reinterpret_cast<const float*>(smem + stage_off(it)) + r;
-            float other[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) other[e] = in[e * D];
-            float* dst = a.dq_acc +
-                         ((size_t)bh * a.Sq_pad + (size_t)iq * kQB + 32 * rank) * D + r;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float own = u2f(rank == 0 ? v0[e] : v1[e]);
-              const float x = rank == 0 ? own + other[e] : other[e] + own;
-              asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)e * D),
-                           "f"(x)
-                           : "memory");
-            }
-          }
-          mbar_arrive(bar(L::kBarQEmpty + it % L::kStages));
-        } else if (!a.deterministic) {
+        if (!a.deterministic) {
           // two 32-column halves, so that only 32 values are live at a time;
           // the columns are released once the second half is read
           float* dst = a.dq_acc + ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
@@ -839,12 +754,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
   }
 
   tc_fence_before();
-  // with pairs, neither CTA leaves while its partner may still write into its
-  // shared memory
-  if (kPair)
-    cluster_sync_all();
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == R::kScoreWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
@@ -893,61 +803,11 @@ __global__ void __launch_bounds__(256) bwd_dq_convert(const BwdArgs a) {
   }
 }
 
-// CTA pairs are built but not dispatched: measured slower at B2 H16 S8192
-// causal (868 against 1,184 TFLOP/s), the exchange making each block's drain
-// longer than the block period.
-constexpr bool kUsePairs = false;
-
-// The atomic-mode D = 128 main kernel in clusters of two CTAs: the units are
-// pairs of kv tiles, and the grid is as many clusters as can be resident at
-// once (up to one per pair unit), two CTAs each.
-static int launch_bwd_pairs(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, bool mod,
-                            cudaStream_t stream) {
-  using L = BwdSmem<128>;
-  constexpr int kThreads = BwdRoles<false>::kThreads;
-  const auto kernel = mod ? bwd_main<128, true, true> : bwd_main<128, false, true>;
-  const int threads = mod ? BwdRoles<true>::kThreads : kThreads;
-  int dev;
-  DeviceInfo info;
-  if (!current_device(&dev, &info) || dev >= 64) return FA_ERR_CUDA;
-  static int max_clusters[64][2] = {};
-  int& mc = max_clusters[dev][mod ? 1 : 0];
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = L::kAllocBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  if (mc == 0) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAllocBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    cfg.gridDim = dim3(info.sm_count & ~1);
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kernel, &cfg) != cudaSuccess || n < 1)
-      return FA_ERR_CUDA;
-    mc = n;
-  }
-  BwdArgs ap = a;
-  ap.n_units = a.B * a.Hkv * ((a.n_ktiles + 1) / 2);
-  const int clusters = ap.n_units < mc ? ap.n_units : mc;
-  cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1));
-  cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, ap) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
-}
+std::atomic<int> g_bwd_kernel{FA_BWD_KERNEL_AUTO};
 
 template <int D>
-static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+static int launch_bwd_d(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream) {
+  const CUtensorMap &tq = m.q, &tk = m.k, &tv = m.v, &tdo = m.dO;
   using L = BwdSmem<D>;
   int dev;
   DeviceInfo info;
@@ -987,11 +847,10 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (a.qblk_rows == 128) {
       const int rc = launch_bwd_main_q128(tq, tk, tv, tdo, a, mod, grid, stream);
       if (rc != FA_OK) return rc;
-    } else if (D == 128 && !a.deterministic && kUsePairs && !mod) {
-      if constexpr (D == 128) {
-        const int rc = launch_bwd_pairs(tq, tk, tv, tdo, a, mod, stream);
-        if (rc != FA_OK) return rc;
-      }
+    } else if (g_bwd_kernel.load(std::memory_order_relaxed) == FA_BWD_KERNEL_PAIR &&
+               bwd_pair_eligible(a, mod)) {
+      const int rc = launch_bwd_main_pair(m, a, stream);
+      if (rc != FA_OK) return rc;
     } else if (a.deterministic) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
@@ -1028,10 +887,9 @@ static int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   return FA_OK;
 }
 
-int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
-  if (a.D == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, a, stream);
-  if (a.D == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, a, stream);
+int launch_bwd(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream) {
+  if (a.D == 128) return launch_bwd_d<128>(m, a, stream);
+  if (a.D == 64) return launch_bwd_d<64>(m, a, stream);
   return FA_ERR_UNSUPPORTED;
 }
 

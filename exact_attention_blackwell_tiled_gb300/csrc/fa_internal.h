@@ -2,6 +2,8 @@
 // libfa.so (argument structs, per-device cache, kernel launchers).
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -135,8 +137,20 @@ struct BwdLayout {
 };
 bool bwd_layout(int B, int Hq, int Sq, int D, int groups, BwdLayout* L);
 
-int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// Tensor maps of a backward call: q and dO in boxes of bwd_qblk_rows rows, k
+// and v in 128-row boxes, and q_half / dO_half in 32-row boxes (the CTA-pair
+// kernel: each CTA of a pair reads its 32 queries of a 64-row block).
+struct BwdMaps {
+  CUtensorMap q, k, v, dO, q_half, dO_half;
+};
+
+int launch_bwd(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream);
+
+// The CTA-pair main kernel (D = 128, atomic dQ, no score modification), and
+// the process-wide kernel choice fa_set_bwd_kernel sets.
+extern std::atomic<int> g_bwd_kernel;
+bool bwd_pair_eligible(const BwdArgs& a, bool mod);
+int launch_bwd_main_pair(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream);
 
 // The backward's query rows per block: 128 (bwd_main_q128) for the
 // deterministic mode at D = 128, 64 (bwd_main) otherwise.  The q and dO tensor

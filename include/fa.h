@@ -162,6 +162,26 @@ int fa_bwd_mod(const void* q, const void* k, const void* v, const void* o, const
 int fa_bwd_status(const void* workspace, fa_stream_t stream);
 
 /*
+ * Backward main kernel for the calls it applies to: head dim 128, atomic dQ
+ * (deterministic == 0) and no score modification beyond the causal mask.
+ *   FA_BWD_KERNEL_AUTO (0, the default): the one-SM kernel.
+ *   FA_BWD_KERNEL_ONE_SM (1): one CTA per kv tile (128 keys), 64-query blocks.
+ *   FA_BWD_KERNEL_PAIR (2): clusters of two CTAs on kv tile pairs (256 keys),
+ *     every product in the 2-CTA MMA mode, the dQ reduction over 256 keys
+ *     before the global fp32 adds (half the adds of the one-SM kernel).
+ *     FlashAttention-4 pages, key contribution #3.  Measured slower than the
+ *     one-SM kernel on GB300, hence not the default.
+ * Other calls ignore the setting.  Process-wide; takes effect at the next
+ * fa_bwd / fa_bwd_mod / fa_bwd_noalloc launch.  Writes the previous setting to
+ * *previous unless it is null.  Returns FA_OK, or FA_ERR_INVALID_ARG (and
+ * changes nothing) for another value of kind.
+ */
+#define FA_BWD_KERNEL_AUTO 0
+#define FA_BWD_KERNEL_ONE_SM 1
+#define FA_BWD_KERNEL_PAIR 2
+int fa_set_bwd_kernel(int kind, int* previous);
+
+/*
  * Split-KV forward: the kv tiles (128 keys each) are cut into n contiguous
  * splits, every (128-row query tile, split) is an independent unit of work, and
  * the splits' partial results are merged by log-sum-exp (fa_lse_merge below).

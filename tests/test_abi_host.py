@@ -215,3 +215,13 @@ def test_python_binding_checks_score_mod_arrays():
         fa._score_mod(True, (-1, 0), None, 2)  # the causal flag and a window together
     # nothing to modify: the plain entry points apply
     assert fa._score_mod(True, None, None, 2) is None
+
+
+def test_bwd_kernel_switch(L):
+    prev = ctypes.c_int(-1)
+    assert L.fa_set_bwd_kernel(2, ctypes.byref(prev)) == 0
+    assert prev.value == 0  # the default: automatic choice
+    assert L.fa_set_bwd_kernel(7, ctypes.byref(prev)) == 1  # rejected, nothing changes
+    assert L.fa_set_bwd_kernel(1, None) == 0
+    assert L.fa_set_bwd_kernel(0, ctypes.byref(prev)) == 0
+    assert prev.value == 1

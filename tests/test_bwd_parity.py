@@ -142,6 +142,42 @@ def test_bwd_workload_sampled_heads():
     _compare(det, ref, w, units)
 
 
+@pytest.fixture
+def pair_kernel():
+    prev = fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR)
+    yield
+    fa.set_bwd_kernel(prev)
+
+
+PAIR_SHAPES = [c for c in SMALL if c[5] == 128] + [
+    (1, 2, 2, 640, 640, 128, True),    # 5 kv tiles: the last pair's second tile holds no key
+    (2, 4, 1, 512, 900, 128, False),   # GQA 4, ragged Sk (8 tiles, the last partial)
+    (1, 1, 1, 1000, 1000, 128, True),  # ragged Sq and Sk, causal union of the pair's blocks
+]
+
+
+@pytest.mark.parametrize("case", PAIR_SHAPES, ids=lambda c: "B%dH%d-%dS%dx%dD%d%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "c" if c[6] else "n"))
+def test_pair_kernel_small_shapes(case, pair_kernel):
+    """The CTA-pair main kernel (2-CTA MMA, dQ reduced over 256 keys before the
+    global adds) against the fp64 backward."""
+    B, Hq, Hkv, Sq, Sk, D, causal = case
+    w = synth.Workload("bwd_pair", B, Hq, Hkv, Sq, Sk, D, causal, 31 + Sq, with_do=True)
+    got, ref, _ = _bwd_case(w, False, guards=True)
+    _compare(got, ref, w)
+
+
+def test_pair_kernel_bwd_workload_sampled_heads(pair_kernel):
+    """The CTA-pair kernel at the backward workload's full size (B=2, H=16,
+    S=8192, causal): two kv heads against the fp64 backward, all outputs finite."""
+    w = synth.BWD
+    units = [3, 2 * w.Hkv - 1]
+    got, ref, _ = _bwd_case(w, False, units=units)
+    _compare(got, ref, w, units)
+    for t in got:
+        assert bool(torch.isfinite(t.float()).all())
+
+
 def test_sq_zero_gives_zero_key_grads():
     k = torch.randn(1, 2, 200, 128, device=DEV).bfloat16()
     v = torch.randn(1, 2, 200, 128, device=DEV).bfloat16()
