@@ -514,15 +514,19 @@ def run_ours(args):
 def run_only(fa, args, dev):
     """One kernel call shape alone, W + K times, nothing else -- the command a
     profiler capture of that kernel runs:
-      --only fwd:S:D:causal        the forward on the sweep workload of that S, D
-      --only bwd:S:D:causal[:det]  the backward (atomic or deterministic dQ) on it
+      --only fwd:S:D:causal             the forward on the sweep workload of that S, D
+      --only bwd:S:D:causal[:det|:pair] the backward on it: atomic dQ, deterministic dQ,
+                                        or atomic on the CTA-pair kernel
     """
     import torch
     parts = args.only.split(":")
     kind, S, D, c = parts[:4]
-    det = len(parts) > 4 and parts[4] == "det"
-    if kind not in ("fwd", "bwd"):
-        raise SystemExit(f"--only: unknown kind {kind!r}")
+    mode = parts[4] if len(parts) > 4 else ""
+    if kind not in ("fwd", "bwd") or mode not in ("", "det", "pair"):
+        raise SystemExit(f"--only: unknown kind or mode {args.only!r}")
+    det = mode == "det"
+    if mode == "pair":
+        fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR)
     w = synth.sweep(int(S), int(D), c in ("1", "c", "causal", "true"))
     gen = torch.Generator(device=dev).manual_seed(w.seed)
     q, k, v, do = (torch.randn(w.B, w.Hq, w.Sq, w.D, device=dev, generator=gen).to(torch.bfloat16)
@@ -553,7 +557,8 @@ def run_only(fa, args, dev):
     ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
     flops = w.flops(backward=(kind == "bwd"))
     print(json.dumps({"only": args.only, "workload": w.name, "B": w.B, "H": w.Hq, "S": w.Sq,
-                      "D": w.D, "causal": w.causal, "deterministic": det, "ms": round(ms, 4),
+                      "D": w.D, "causal": w.causal, "deterministic": det,
+                      "bwd_kernel": "pair" if mode == "pair" else "default", "ms": round(ms, 4),
                       "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}), flush=True)
 
 
