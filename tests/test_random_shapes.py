@@ -58,13 +58,21 @@ def test_random_shape(seed):
     dq_r, dk_r, dv_r, o_r, lse_r = oracle.bwd_mod(q, k, v, do, w.softmax_scale, wl, wr,
                                                   slopes=slopes)
     assert_fwd_close(o, lse, o_r, lse_r, name)
-    for det in (False, True):
+    # atomic, deterministic, and atomic with the CTA-pair kernel selected (it
+    # runs where it applies: D = 128 without a window other than causal or a
+    # bias; elsewhere the call takes the default kernel)
+    for mode in ("atomic", "det", "pair"):
+        det = mode == "det"
         ws = torch.empty(fa.bwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, det), dtype=torch.uint8,
                          device=DEV)
-        dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, scale=w.softmax_scale, deterministic=det,
-                            workspace=ws, **kw)
-        assert fa.bwd_status(ws) == fa.FA_OK
-        tag = f"{name} det={det}"
+        prev = fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR if mode == "pair" else fa.BWD_KERNEL_AUTO)
+        try:
+            dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, scale=w.softmax_scale, deterministic=det,
+                                workspace=ws, **kw)
+            assert fa.bwd_status(ws) == fa.FA_OK
+        finally:
+            fa.set_bwd_kernel(prev)
+        tag = f"{name} {mode}"
         if wl == 0 and wr == 0:
             bound = 1e-3 * float(np.abs(dv_r).max())
             assert float(dq.float().abs().max()) <= bound, f"{tag} dQ"
