@@ -190,6 +190,20 @@ def test_sq_zero_gives_zero_key_grads():
     assert bool((dk == 0).all()) and bool((dv == 0).all())
 
 
+def test_pair_kernel_sq_zero_gives_zero_key_grads(pair_kernel):
+    """With no queries every pair unit has no block: the pair kernel still loads
+    K / V and writes dK = dV = 0, including an odd kv-tile count (3 tiles)."""
+    k = torch.randn(1, 2, 300, 128, device=DEV).bfloat16()
+    v = torch.randn(1, 2, 300, 128, device=DEV).bfloat16()
+    q = torch.empty(1, 2, 0, 128, device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty(1, 2, 0, device=DEV)
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    _, dk, dv = fa.bwd(q, k, v, q, q, lse, causal=True, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert bool((dk == 0).all()) and bool((dv == 0).all())
+
+
 def test_timeout_status_is_clear_after_normal_runs():
     w = synth.Workload("st", 1, 2, 2, 256, 256, 64, True, 1, with_do=True)
     got, ref, (qd, kd, vd, o, dod, lse, ws) = _bwd_case(w, False)
