@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_q128.cu", "fa_bwd_pair.cu", "fa_merge.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_ring.cu", "fa_bwd.cu", "fa_bwd_q128.cu", "fa_bwd_pair.cu", "fa_merge.cu", "fa_noalloc.cu"]
 HEADERS = ["fa_internal.h", "ptx.cuh", "exp2.cuh", "bwd_common.cuh", "fwd_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -679,6 +679,12 @@ static int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // kernel
   const bool plain_window = a.wl < 0 && (a.wr < 0 || (a.wr == 0 && a.causal));
   const int mode = a.alibi ? 2 : ((plain_window && !a.seqlens_k) ? 0 : 1);
+  if (fwd_ring64_eligible(a, D, mode)) {
+    if (launch_fwd_ring64(tq, tk, tv, a, grid, stream) != FA_OK) return FA_ERR_CUDA;
+    record_timing(true, stream);
+    note_launches(1);
+    return FA_OK;
+  }
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs);
   const KernelFn kernels[2][3] = {{fwd_kernel<D, 0, false>, fwd_kernel<D, 1, false>,
                                    fwd_kernel<D, 2, false>},

@@ -63,6 +63,14 @@ struct FwdArgs {
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdArgs& a, int D, cudaStream_t stream);
 
+// The D = 64 forward with a ring of score buffers per query tile, for no mask or
+// the causal one, a positive scale and no split (mode 0 of the forward: no
+// window, bias or key counts).  `a` comes filled in by the forward's launcher
+// (schedule, status pointer); `grid` CTAs.
+bool fwd_ring64_eligible(const FwdArgs& a, int D, int mode);
+int launch_fwd_ring64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const FwdArgs& a, int grid, cudaStream_t stream);
+
 
 // Log-sum-exp merge of n attention parts over disjoint key sets.
 struct MergeArgs {

@@ -64,6 +64,25 @@ def test_small_shapes(case):
     _run_full(B, Hq, Hkv, Sq, Sk, D, causal, seed=hash(case) % 1000)
 
 
+# The D = 64 forward without modifications walks each 128-key tile as two
+# 64-key halves through a ring of three score buffers per query tile, and keeps
+# that ring (and its barrier phases) running from one unit to the next.
+RING64 = [
+    (1, 2, 2, 200, 60, 64, False),     # second half of the only kv tile sees no key
+    (1, 2, 2, 300, 65, 64, True),      # one key in the second half
+    (1, 3, 3, 200, 192, 64, True),     # tile 1 of the pair sees one more kv tile
+    (2, 40, 40, 640, 640, 64, True),   # 240 units: several per CTA, causal
+    (2, 40, 8, 384, 1000, 64, False),  # 160 units, GQA 5, ragged keys
+]
+
+
+@pytest.mark.parametrize("case", RING64, ids=lambda c: "B%dH%d-%dS%dx%dD%d%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "c" if c[6] else "n"))
+def test_d64_score_ring_shapes(case):
+    B, Hq, Hkv, Sq, Sk, D, causal = case
+    _run_full(B, Hq, Hkv, Sq, Sk, D, causal, seed=hash(case) % 1000)
+
+
 def test_tiny_workload_full():
     """The tiny workload (B=1, H=2, S=256, D=64, non-causal, scale 1/8) in full."""
     w = synth.TINY
