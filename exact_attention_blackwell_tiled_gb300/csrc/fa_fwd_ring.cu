@@ -12,9 +12,14 @@
 // owns a ring of three 64-column score buffers in tensor memory:
 //   GEMM 1 (k):  S_t[k mod 3] = Q_t K_half(k)^T        (SS, N = 64)
 //   GEMM 2 (k):  O_t += P_t[k mod 3] V_half(k)         (TS, P read from TMEM)
-// GEMM 1 of half k+3 is issued as soon as GEMM 2 of half k is done with the
-// buffer, so while the softmax warps work on half k the scores of halves k+1
-// and k+2 are already in TMEM or being computed, and the softmax runs back to back instead of waiting
+// GEMM 1 of a half is issued as soon as GEMM 2 of the half three back is done
+// with its buffer, so while the softmax warps work on half k the scores of
+// halves k+1 and k+2 are already in TMEM or being computed.  GEMM 1 works per K
+// tile: when the tile's two halves land in adjacent buffers (two tiles in
+// three) one N = 128 group computes both at the full MMA rate (64 cycles per
+// instruction); two N = 64 groups hold the tensor pipe about 2.8 times as long
+// (about 89 cycles per N = 64 instruction measured in this kernel's mix).  The
+// softmax then runs back to back instead of waiting
 // for a GEMM 2 -> GEMM 1 round trip after every block (FlashAttention-4 pages:
 // the per-tile phases GEMM 1 -> softmax -> GEMM 2 and the pipeline that overlaps
 // the softmax of one block with GEMM 2 of the previous and GEMM 1 of the next).
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     if (lane == 0) {
       const int t = warp - 9;
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, 64, false, false);
+      constexpr uint32_t kIdescS2 = idesc_bf16_f32(kTile, 128, false, false);
       constexpr uint32_t kHi = sdesc_hi(1024);  // SBO 1024 B, version 1, 128B swizzle
       const uint32_t s_cols = tmem + t * L::kColsPerTile;
       uint32_t k_it = 0, q_it = 0;
@@ -235,30 +241,49 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         if (n == 0) mbar_arrive(bar(L::kBarQEmpty + qs));
         const uint32_t q_lo = sdesc_lo(sbase + L::kOffQ + (2 * qs + t) * L::kTileBytes, 16);
         const uint32_t kbase = k_it;  // ring position of K_jlo
-        for (int k = 0; ok && k < n; ++k) {
-          const int i = k >> 1, hf = k & 1;
+        // buffer of the score half with global index g is free once GEMM 2 of
+        // half g - 3 is done; that barrier is within one phase: this thread
+        // waited for the buffer's use before that one before GEMM 1 of g - 3
+        auto buf_free = [&](uint32_t g) -> bool {
+          return g < (uint32_t)L::kRing ||
+                 mbar_wait(bar(L::kBarODone + t * L::kRing + g % L::kRing),
+                           (g / L::kRing - 1) & 1, abort_flag);
+        };
+        for (int i = 0; ok && i < m; ++i) {
           const uint32_t pos = kbase + i, st = pos % L::kKStages;
-          const uint32_t b = gs % L::kRing;
-          // the buffer is free once GEMM 2 of its previous half (gs - 3) is
-          // done; that barrier is within one phase: this thread waited for
-          // the buffer's use before that one before issuing GEMM 1 of gs - 3
-          ok = (gs < (uint32_t)L::kRing ||
-                mbar_wait(bar(L::kBarODone + t * L::kRing + b), (gs / L::kRing - 1) & 1,
-                          abort_flag)) &&
-               (hf == 1 || mbar_wait(bar(L::kBarKFull + st), (pos / L::kKStages) & 1, abort_flag));
+          const uint32_t b0 = gs % L::kRing;
+          // both halves of K tile i; when their buffers are adjacent (b0 < 2)
+          // one N = 128 group computes both, at the full MMA rate
+          ok = mbar_wait(bar(L::kBarKFull + st), (pos / L::kKStages) & 1, abort_flag) &&
+               buf_free(gs) && buf_free(gs + 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d = s_cols + 64 * b;
-          const uint32_t k_lo =
-              sdesc_lo(sbase + L::kOffK + st * L::kTileBytes + hf * L::kHalfBytes, 16);
-          umma_ss_w<0>(d, q_lo, kHi, k_lo, kHi, kIdescS);
+          const uint32_t k_tile = sbase + L::kOffK + st * L::kTileBytes;
+          if (b0 + 1 < (uint32_t)L::kRing) {
+            const uint32_t d = s_cols + 64 * b0;
+            const uint32_t k_lo = sdesc_lo(k_tile, 16);
+            umma_ss_w<0>(d, q_lo, kHi, k_lo, kHi, kIdescS2);
 #pragma unroll
-          for (int kk = 1; kk < D / 16; ++kk)
-            umma_ss_w<1>(d, q_lo + kk * 2, kHi, k_lo + kk * 2, kHi, kIdescS);
-          umma_commit(bar(L::kBarSFull + t * L::kRing + b));
-          ++gs;
-          if (hf == 1) umma_commit(bar(L::kBarKEmpty + st));
-          if (k == n - 1) umma_commit(bar(L::kBarQEmpty + qs));
+            for (int kk = 1; kk < D / 16; ++kk)
+              umma_ss_w<1>(d, q_lo + kk * 2, kHi, k_lo + kk * 2, kHi, kIdescS2);
+            umma_commit(bar(L::kBarSFull + t * L::kRing + b0));
+            umma_commit(bar(L::kBarSFull + t * L::kRing + b0 + 1));
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const uint32_t b = (b0 + hf) % L::kRing;
+              const uint32_t d = s_cols + 64 * b;
+              const uint32_t k_lo = sdesc_lo(k_tile + hf * L::kHalfBytes, 16);
+              umma_ss_w<0>(d, q_lo, kHi, k_lo, kHi, kIdescS);
+#pragma unroll
+              for (int kk = 1; kk < D / 16; ++kk)
+                umma_ss_w<1>(d, q_lo + kk * 2, kHi, k_lo + kk * 2, kHi, kIdescS);
+              umma_commit(bar(L::kBarSFull + t * L::kRing + b));
+            }
+          }
+          gs += 2;
+          umma_commit(bar(L::kBarKEmpty + st));
+          if (i == m - 1) umma_commit(bar(L::kBarQEmpty + qs));
         }
         // this tile's share of the K tiles only the other tile reaches, each
         // once it has landed
@@ -365,9 +390,13 @@ __global__ void __launch_bounds__(kRingThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (kv0 + i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        float mraw = -INFINITY;
+        // four independent max chains (shorter dependency chains)
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) mraw = fmax3(mraw, u2f(v[i]), u2f(v[i + 1]));
+        for (int i = 0; i < 64; i += 8)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mq[j] = fmax3(mq[j], u2f(v[i + 2 * j]), u2f(v[i + 2 * j + 1]));
+        float mraw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         if (mraw != -INFINITY) mraw *= c;
         // Conditional rescale: keep a stale running max unless the new max
         // exceeds it by more than 8 (P then stays <= 2^8).
@@ -382,7 +411,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         }
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         const float2 nm2 = make_float2(neg_m, neg_m);
-        float2 sum2 = make_float2(0.f, 0.f);
+        float2 sum2 = make_float2(0.f, 0.f), sum2b = make_float2(0.f, 0.f);
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -394,12 +423,15 @@ __global__ void __launch_bounds__(kRingThreads, 1)
           } else {
             p0 = ex2_mufu(tt.x), p1 = ex2_mufu(tt.y);
           }
-          sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+          if (i & 1)
+            sum2b = __fadd2_rn(sum2b, make_float2(p0, p1));
+          else
+            sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         __syncwarp();
         tmem_st32(t_row + 64 * b, pk);
-        l_run = l_run * alpha + (sum2.x + sum2.y);
+        l_run = l_run * alpha + ((sum2.x + sum2b.x) + (sum2.y + sum2b.y));
         if (__any_sync(0xffffffffu, rescale)) {
           // GEMM 2 of the previous half (global half x-2) must be done before O
           // is rescaled; GEMM 2 of this half waits for this thread's P
