@@ -51,7 +51,8 @@
 // of part p, which then write their c/2 columns of P^T and c/2 of dS^T over
 // them (P^T at cp, dS^T at cp+c/2), so the parts never touch each other's
 // columns;
-// dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
+// dP^T [128,192), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D); at D = 64
+// a second dP^T buffer [384,448) takes the odd blocks.
 // Three issuing threads: a thread that has MMAs queued and then waits on a
 // barrier only continues once the tensor core has taken those MMAs, so a lone
 // issuer lets the tensor core run dry at every wait and delays its own view of
@@ -202,8 +203,11 @@ struct BwdSmem {
   // P^T / dS^T published, one barrier per block parity: a waiter may lag the
   // softmax warps by a block, never by two blocks of the same parity
   static constexpr int kBarPReady = kBarSFull + 2;   // 2
-  static constexpr int kBarDPFull = kBarPReady + 2;
-  static constexpr int kBarDSReady = kBarDPFull + 1;  // 2
+  // dP^T buffers: two at D = 64, which leaves the TMEM columns for a second
+  // one, so that dP^T(i+1) need not wait for the softmax warps to read dP^T(i)
+  static constexpr int kDPBufs = (D == 64) ? 2 : 1;
+  static constexpr int kBarDPFull = kBarPReady + 2;   // kDPBufs
+  static constexpr int kBarDSReady = kBarDPFull + kDPBufs;  // 2
   static constexpr int kBarDQFull = kBarDSReady + 2;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQEmpty + 1;
@@ -217,6 +221,11 @@ struct BwdSmem {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256,
                             kColDK = 256 + D;
+  static constexpr uint32_t kColDP1 = 256 + 2 * D;  // second dP^T buffer (D = 64)
+  static_assert(kDPBufs == 1 || kColDP1 + kQB <= kTmemCols, "second dP^T buffer");
+  static __device__ __forceinline__ uint32_t col_dp(uint32_t it) {
+    return (kDPBufs == 2 && (it & 1)) ? kColDP1 : kColDP;
+  }
 };
 
 // kMod: a sliding window and / or the relative-position bias (a.alibi); the
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       mbar_init(bar(L::kBarPReady + s), R::kSmxThreads);
       mbar_init(bar(L::kBarDSReady + s), R::kSmxThreads);
     }
-    mbar_init(bar(L::kBarDPFull), 1);
+    for (int s = 0; s < L::kDPBufs; ++s) mbar_init(bar(L::kBarDPFull + s), 1);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKVFull), 1);
@@ -392,15 +401,17 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
               issue_kmajor(tmem + L::kColS + (it & 1) * kQB, k_lo, sdesc_lo(q_base, 16));
               umma_commit(bar(L::kBarSFull + (it & 1)));
             } else {
-              // the dP^T columns are free once the softmax warps have read dP^T(it-1)
-              if (it >= 1 && !mbar_wait(bar(L::kBarDSReady + ((it - 1) & 1)),
-                                        ((it - 1) >> 1) & 1, abort_flag)) {
+              // the dP^T buffer is free once the softmax warps have read the
+              // dP^T it held before (block it - kDPBufs)
+              constexpr uint32_t kNB = L::kDPBufs;
+              if (it >= kNB && !mbar_wait(bar(L::kBarDSReady + ((it - kNB) & 1)),
+                                          ((it - kNB) >> 1) & 1, abort_flag)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_kmajor(tmem + L::kColDP, v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
-              umma_commit(bar(L::kBarDPFull));
+              issue_kmajor(tmem + L::col_dp(it), v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
+              umma_commit(bar(L::kBarDPFull + it % kNB));
             }
           }
           // K and V may be replaced once both sides are done with them
@@ -560,12 +571,15 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           const float4 x = s_delta[q];
           dl[4 * q] = x.x, dl[4 * q + 1] = x.y, dl[4 * q + 2] = x.z, dl[4 * q + 3] = x.w;
         }
-        if (!warp_wait_b(bar(L::kBarDPFull), it & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait_b(bar(L::kBarDPFull + it % L::kDPBufs), (it / L::kDPBufs) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         uint32_t wbuf[kSC / 2];
         {
           uint32_t v[kSC];
-          tmem_ld<kSC>(t_row + L::kColDP + c0, v);
+          tmem_ld<kSC>(t_row + L::col_dp(it) + c0, v);
 #pragma unroll
           for (int e = 0; e < kSC / 2; ++e) {
             const float d0 = p[2 * e] * (u2f(v[2 * e]) - dl[2 * e]);
