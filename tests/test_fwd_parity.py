@@ -89,11 +89,13 @@ def test_tiny_workload_full():
     _run_full(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed, scale=w.scale)
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("scale", [0.0, 1.0, 4.0])
-def test_scale_extremes(scale):
+def test_scale_extremes(scale, D):
     """scale 0 (uniform weights), and peaky softmax rows that stress the
-    conditional rescale."""
-    _run_full(1, 2, 2, 384, 384, 128, True, seed=11, scale=scale, qk_std=2.0)
+    conditional rescale (at D = 64 the rescale waits for the previous half's
+    GEMM 2 through its score buffer's barrier)."""
+    _run_full(1, 2, 2, 384, 384, D, True, seed=11, scale=scale, qk_std=2.0)
 
 
 def test_sq_zero_is_noop():
@@ -142,7 +144,7 @@ def test_gqa_spike_sampled():
 
 
 @pytest.mark.parametrize("S,D,causal", [(1024, 64, True), (4096, 128, False), (8192, 128, False),
-                                        (16384, 64, True), (32768, 128, False)])
+                                        (8192, 64, False), (16384, 64, True), (32768, 128, False)])
 def test_sweep_sampled(S, D, causal):
     _sampled(synth.sweep(S, D, causal), 16 if S >= 16384 else 48, 0)
 
