@@ -44,8 +44,10 @@
 //   warp n+4      TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i
 //                 per block into a 3-stage ring;
 //   warp n+5      TMEM owner; one thread issues S^T;
-//   warp n+6      one thread issues dP^T;
-//   warp n+7      one thread issues dV, dK and dQ^T.
+//   warp n+6      one thread issues dP^T (and, at D = 64 with atomic dQ, dQ^T
+//                 of the previous block behind it);
+//   warp n+7      one thread issues dV, dK and dQ^T (dV and dK where warp n+6
+//                 issues dQ^T).
 // TMEM columns: S^T double buffer [0,64) [64,128); P^T and dS^T (bf16 pairs)
 // replace it in place: query columns cp..cp+c-1 of S^T are read by the warps
 // of part p, which then write their c/2 columns of P^T and c/2 of dS^T over
@@ -66,8 +68,11 @@
 // warps write buffer i%3 only after S^T(i) is complete, which the S^T issuer
 // started after dK(i-2), which the gradient issuer started after dQ^T(i-3), the
 // buffer's previous reader; the tensor core completes one thread's MMAs in
-// order, so no separate hand-back is needed.  At D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K
-// block twice; lanes 64-127 of its result are ignored.
+// order, so no separate hand-back is needed.  Where the dP^T thread issues
+// dQ^T, its order is dP^T(i-1), dQ^T(i-2), dP^T(i): dP^T(i) complete, which the
+// softmax warps see before they write dS^T(i), implies dQ^T(i-2) complete.  At
+// D = 64 the dQ^T MMA runs with M = 128 by reading the 64-column K block twice;
+// lanes 64-127 of its result are ignored.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -362,12 +367,38 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
       constexpr uint32_t kHi = sdesc_hi(1024);
       const int role = warp - R::kScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
+      // who issues dQ^T: the gradient thread after dK, or at D = 64 with atomic
+      // dQ the dP^T thread, behind dP^T of the next block (measured: D = 64
+      // atomic +5 to +7%, D = 128 -12%, the D = 64 deterministic mode -1 to -3%)
+      const bool dq_on_dp = (D == 64) && !a.deterministic;
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
         const BwdUnit w = unit_of(u);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        // dQ^T(j) = K^T dS^T(j) (M = head dim, K = keys) once the softmax warps
+        // have published dS^T(j) (waited here when wait_ds) and the drain has
+        // emptied the dQ^T columns of block j-1
+        auto issue_dq = [&](uint32_t j, bool wait_ds) -> bool {
+          if (wait_ds && !mbar_wait(bar(L::kBarDSReady + (j & 1)), (j >> 1) & 1, abort_flag))
+            return false;
+          if (j > 0 && !mbar_wait(bar(L::kBarDQEmpty), (j - 1) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t kt_lo = sdesc_lo(sbase + L::kOffK, kLboKT);
+          const uint32_t dsb_lo =
+              sdesc_lo(sbase + L::kOffDS, 1024) + (((j % L::kDSBufs) * L::kDSBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t ko = (kk * 16 * 128) >> 4;
+            if (kk == 0)
+              umma_ss_w<0>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
+            else
+              umma_ss_w<1>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
+          }
+          umma_commit(bar(L::kBarDQFull));
+          return true;
+        };
         if (role < 2) {
           // ---- S^T(i) = K Q_i^T or dP^T(i) = V dO_i^T, both operands K-major
           const uint32_t k_lo = sdesc_lo(sbase + L::kOffK, 16);
@@ -412,14 +443,19 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
               tc_fence_after();
               issue_kmajor(tmem + L::col_dp(it), v_lo, sdesc_lo(q_base + L::kQTileBytes, 16));
               umma_commit(bar(L::kBarDPFull + it % kNB));
+              // dQ^T of the unit's previous block, behind dP^T of this one
+              if (dq_on_dp && t > 0 && !issue_dq(it - 1, true)) {
+                ok = false;
+                break;
+              }
             }
           }
+          // the unit's last dQ^T, before K may be replaced
+          if (ok && dq_on_dp && role == 1 && w.n_it > 0) ok = issue_dq(it - 1, true);
           // K and V may be replaced once both sides are done with them
           if (ok) umma_commit(bar(L::kBarKVEmpty));
         } else {
-          // ---- dV += P^T dO, dK += dS^T Q (A from TMEM), dQ^T = K^T dS^T
-          const uint32_t kt_lo = sdesc_lo(sbase + L::kOffK, kLboKT);
-          const uint32_t ds_lo = sdesc_lo(sbase + L::kOffDS, 1024);
+          // ---- dV += P^T dO, dK += dS^T Q (A from TMEM)
           // dV / dK accumulators are free once the previous unit's epilogue
           // has read them
           if (unit > 0 && !mbar_wait(bar(L::kBarDKVEmpty), (unit - 1) & 1, abort_flag)) {
@@ -464,23 +500,10 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
             // can be reused
             umma_commit(bar(L::kBarQEmpty + it % L::kStages));
             umma_commit(bar(L::kBarSFree + (it & 1)));
-            // dQ^T = K^T dS^T (M = head dim, K = keys) once the drain of the
-            // previous block has emptied the dQ^T columns
-            if (it > 0 && !mbar_wait(bar(L::kBarDQEmpty), (it - 1) & 1, abort_flag)) {
+            if (!dq_on_dp && !issue_dq(it, false)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint32_t dsb_lo = ds_lo + (((it % L::kDSBufs) * L::kDSBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t ko = (kk * 16 * 128) >> 4;
-              if (kk == 0)
-                umma_ss_w<0>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
-              else
-                umma_ss_w<1>(tmem + L::kColDQ, kt_lo + ko, kHi, dsb_lo + ko, kHi, kIdDQ);
-            }
-            umma_commit(bar(L::kBarDQFull));
           }
           if (ok) {
             umma_commit(bar(L::kBarKVEmpty));
