@@ -16,8 +16,9 @@
 // HBM-bound: per row it reads n * (4 * D + 4) bytes and writes 2 * D + 4.  One
 // warp per row; the part LSEs are read lane-strided and reduced with shuffles,
 // and lane l owns the D/32 contiguous elements [l * D/32, ...) of every part
-// row (16-byte loads at D = 128).  With at most 32 parts, lane c computes part
-// c's weight once and the weighted part rows are loaded eight at a time, so a
+// row (16-byte loads at D = 128).  With at most eight parts every part row is
+// loaded together with the LSEs; with at most 32, lane c computes part c's
+// weight once and the weighted part rows are loaded eight at a time, so a
 // warp keeps eight independent loads in flight instead of one.
 #include <cuda_bf16.h>
 
@@ -71,8 +72,27 @@ __device__ __forceinline__ Vec<D / 32> load_part(const MergeArgs& m, int c, long
   return x;
 }
 
+// Lane l's D/32 merged elements of a row as bf16, and the row's LSE.
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32)
+__device__ __forceinline__ void store_row(const MergeArgs& m, long long row, int lane,
+                                          const float* acc, float lse) {
+  constexpr int kV = D / 32;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(m.o) + (size_t)row * D + lane * kV;
+  if (kV == 4) {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&p0);
+    w.y = *reinterpret_cast<const uint32_t*>(&p1);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0], acc[1]);
+  }
+  if (lane == 0) m.lse[row] = lse;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32, 4)
     merge_kernel(const MergeArgs m) {
   constexpr int kV = D / 32;  // elements per lane
   constexpr int kBatch = 8;   // part rows in flight per warp
@@ -81,6 +101,36 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const long long warps = (long long)gridDim.x * kMergeWarps;
   for (long long row = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5); row < m.rows;
        row += warps) {
+    if (m.n <= kBatch) {
+      // up to eight parts: the part rows are loaded together with the LSEs (one
+      // round trip per row instead of two); an empty part's row, which its
+      // split did not write, is loaded but given no weight
+      const float l0 = lane < m.n ? m.lse_part[(size_t)lane * m.rows + row] : -INFINITY;
+      Vec<kV> x[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) x[u] = load_part<D>(m, u, row, lane, u < m.n);
+      const float M = warp_max(l0);
+      float acc[kV];
+#pragma unroll
+      for (int e = 0; e < kV; ++e) acc[e] = 0.f;
+      float lse = -INFINITY;
+      if (M != -INFINITY) {
+        const float p = expf(l0 - M);  // 0 for an empty part
+        const float z = warp_sum(p);
+        lse = M + logf(z);
+        const float wl = p / z;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, u);
+          if (u < m.n && w != 0.f) {
+#pragma unroll
+            for (int e = 0; e < kV; ++e) acc[e] = fmaf(w, x[u].e[e], acc[e]);
+          }
+        }
+      }
+      store_row<D>(m, row, lane, acc, lse);
+      continue;
+    }
     // part LSEs, lane-strided; lane c keeps part c's (the common n <= 32 case)
     const float l0 = lane < m.n ? m.lse_part[(size_t)lane * m.rows + row] : -INFINITY;
     float M = l0;
@@ -124,18 +174,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         }
       }
     }
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(m.o) + (size_t)row * D + lane * kV;
-    if (kV == 4) {
-      const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-      const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-      uint2 w;
-      w.x = *reinterpret_cast<const uint32_t*>(&p0);
-      w.y = *reinterpret_cast<const uint32_t*>(&p1);
-      *reinterpret_cast<uint2*>(dst) = w;
-    } else {
-      *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0], acc[1]);
-    }
-    if (lane == 0) m.lse[row] = lse;
+    store_row<D>(m, row, lane, acc, lse);
   }
 }
 
