@@ -89,6 +89,13 @@ int check_device() {
   DeviceInfo info;
   if (!current_device(&dev, &info)) return FA_ERR_CUDA;
   if (info.cc_major != 10 || info.cc_minor != 3) return FA_ERR_UNSUPPORTED;
+  // The tensor maps are encoded through the driver API, which needs a context
+  // current on the calling thread.  The runtime binds its primary context to a
+  // thread lazily (at the first call that needs it), so on a thread that has
+  // made no such call yet -- a framework's worker thread whose allocations were
+  // all served from a cache, say -- the encoder failed with
+  // CUDA_ERROR_INVALID_CONTEXT.  Selecting the current device again binds it.
+  if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 

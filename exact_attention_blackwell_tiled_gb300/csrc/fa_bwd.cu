@@ -44,8 +44,8 @@
 //   warp n+4      TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i
 //                 per block into a 3-stage ring;
 //   warp n+5      TMEM owner; one thread issues S^T;
-//   warp n+6      one thread issues dP^T (and, at D = 64 with atomic dQ, dQ^T
-//                 of the previous block behind it);
+//   warp n+6      one thread issues dP^T (and, at D = 64, dQ^T of the previous
+//                 block behind it);
 //   warp n+7      one thread issues dV, dK and dQ^T (dV and dK where warp n+6
 //                 issues dQ^T).
 // TMEM columns: S^T double buffer [0,64) [64,128); P^T and dS^T (bf16 pairs)
@@ -367,10 +367,12 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       constexpr uint32_t kLboKT = (D == 128) ? (uint32_t)L::kKVBlockBytes : 0u;
       constexpr uint32_t kHi = sdesc_hi(1024);
       const int role = warp - R::kScoreWarp;  // 0: S^T, 1: dP^T, 2: gradients
-      // who issues dQ^T: the gradient thread after dK, or at D = 64 with atomic
-      // dQ the dP^T thread, behind dP^T of the next block (measured: D = 64
-      // atomic +5 to +7%, D = 128 -12%, the D = 64 deterministic mode -1 to -3%)
-      const bool dq_on_dp = (D == 64) && !a.deterministic;
+      // who issues dQ^T: the gradient thread after dK, or at D = 64 the dP^T
+      // thread, behind dP^T of the next block (measured: D = 64 atomic +5 to
+      // +7%, its deterministic mode 0 to -3%, D = 128 -12%).  A compile-time
+      // choice: testing the mode at run time in the issuing loops cost the
+      // atomic mode 2-3%.
+      constexpr bool dq_on_dp = (D == 64);
       uint32_t it = 0, unit = 0;
       bool ok = true;
       for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
