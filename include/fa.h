@@ -26,6 +26,11 @@
  * on `stream` (0 = legacy default stream); results are valid after the stream
  * is synchronised.
  *
+ * Threads: any host thread may call, on the device current for that thread
+ * (the runtime's cudaGetDevice).  Each call makes that device's primary context
+ * current on the calling thread before it builds its tensor maps, so a thread
+ * that has made no CUDA call of its own yet is served as well.
+ *
  * Errors: arguments are validated on the host before anything is launched; on
  * a validation error nothing is written and a status code is returned.  Launch
  * failures return FA_ERR_CUDA.  Device-side waits carry an iteration/time cap;
