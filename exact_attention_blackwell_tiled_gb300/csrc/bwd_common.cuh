@@ -181,7 +181,9 @@ struct BwdUnit {
   int kv_len;  // keys of batch b
 };
 
-// The r-th unit this CTA processes (-1 when it has no more).  Units are either
+// The r-th unit this CTA processes under static dealing (-1 when it has no
+// more; with a.dyn the units come from a global counter instead, in the order
+// bwd_unit decodes: groups of a.head_group kv heads, kv tile major).  Units are either
 // head-major (u = bhk * n_ktiles + j, round robin, so CTAs running together
 // share the queries of few heads in L2; non-causal and windowed calls) or,
 // with causal masking, ordered by ascending kv tile (the longest units first)
@@ -208,7 +210,15 @@ __device__ __forceinline__ int bwd_cta_unit_pair(const BwdArgs& a, int r) {
 template <bool kMod, int QB>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdArgs& a, int u, int group) {
   BwdUnit w;
-  if (a.snake) {
+  if (a.dyn) {
+    // groups of head_group kv heads in turn; in a group, kv tile major
+    const int nbhk = a.B * a.Hkv, G = a.head_group, nk = a.n_ktiles;
+    const int g = u / (G * nk), h0 = g * G;
+    const int gg = min(G, nbhk - h0);
+    const int r = u - g * G * nk;
+    w.j = r / gg;
+    w.bhk = h0 + (r - w.j * gg);
+  } else if (a.snake) {
     const int nbhk = a.B * a.Hkv;
     w.j = u / nbhk;
     w.bhk = u - w.j * nbhk;

@@ -491,6 +491,16 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // an ascending chain: reversed, it would deal the shortest units first and
   // leave a tail.
   a.desc = (a.deterministic && !a.snake) ? 1 : 0;
+  a.unit_counter = reinterpret_cast<int*>(ws + L.off_status + 128);  // header, own line
+  {
+    // kv heads per group of the dynamic dealing: q, dO (bf16) and the dQ
+    // accumulators (fp32, one per group) of the kv head's q heads, plus K, V
+    const double per_kv_head = (double)(Hq / Hkv) * Sq * D * (4.0 + 4.0 * groups) +
+                               (double)Sk * D * 4.0;
+    int hg = (int)(kBwdGroupBytes / (per_kv_head > 1.0 ? per_kv_head : 1.0));
+    if (hg > B * Hkv) hg = B * Hkv;
+    a.head_group = hg < 1 ? 1 : hg;
+  }
   a.dq_groups = groups;
   a.dq_group_stride = (size_t)B * Hq * a.Sq_pad * D;
   a.sem_group_stride = B * Hq * a.n_qblk;

@@ -101,6 +101,9 @@ struct BwdRoles {
   static constexpr int kGradWarp = kScoreWarp + 2;  // dV / dK / dQ^T issuer
   static constexpr int kThreads = 32 * (kGradWarp + 1);
   static constexpr int kSmxThreads = 32 * kSmxWarps;
+  // readers of a dynamically dealt unit: every softmax and drain warp, and the
+  // three issuing threads (the TMA thread takes the units)
+  static constexpr int kUnitReaders = kSmxWarps + 4 + 3;
   static_assert(kSmxCols == 16 || kSmxCols == 32, "softmax warp column split");
   static_assert(kDrainWarp0 % 4 == 0, "drain warp q reads TMEM lane quarter q");
 };
@@ -179,7 +182,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const BwdArgs a) {
   for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < nsem;
        s += (long long)gridDim.x * blockDim.x)
     a.sem[s] = 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *a.status = 0;
+    *a.unit_counter = 0;
+  }
 }
 
 // ------------------------------------------------------------------ main kernel
@@ -219,9 +225,14 @@ struct BwdSmem {
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
   static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
-  static constexpr int kNumBars = kBarDrain + 3;
+  // dynamic dealing: a ring of unit numbers taken by the TMA thread
+  static constexpr int kURing = 8;
+  static constexpr int kBarUFull = kBarDrain + 3;      // kURing
+  static constexpr int kBarUEmpty = kBarUFull + kURing;  // kURing
+  static constexpr int kNumBars = kBarUEmpty + kURing;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kOffURing = kOffMisc + 16;
+  static constexpr int kBytes = kOffURing + 4 * kURing;
   static constexpr int kAllocBytes = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256,
@@ -274,6 +285,10 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     mbar_init(bar(L::kBarDKVEmpty), 128);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFree + s), 1);
     for (int s = 0; s < 3; ++s) mbar_init(bar(L::kBarDrain + s), 1);
+    for (int s = 0; s < L::kURing; ++s) {
+      mbar_init(bar(L::kBarUFull + s), 1);
+      mbar_init(bar(L::kBarUEmpty + s), R::kUnitReaders);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -296,7 +311,32 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
   grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
-  auto next_unit = [&](int r) { return bwd_cta_unit(a, r); };
+  // The r-th unit of this CTA.  Static dealing: computed by every role alike.
+  // Dynamic dealing: the TMA thread takes the next unit number from the global
+  // counter and posts it in ring slot r % kURing (take_unit); the other roles
+  // read it there (read_unit; warp_wide: all lanes of the warp read, lane 0
+  // hands the slot back).  -1 ends the walk.
+  volatile int* uring = reinterpret_cast<volatile int*>(smem + L::kOffURing);
+  auto take_unit = [&](int r) -> int {
+    if (!a.dyn) return bwd_cta_unit(a, r);
+    const int s = r % L::kURing;
+    if (!mbar_wait(bar(L::kBarUEmpty + s), ((r / L::kURing) & 1) ^ 1, abort_flag)) return -1;
+    int u = atomicAdd(a.unit_counter, 1);
+    if (u >= a.n_units) u = -1;
+    uring[s] = u;
+    mbar_arrive(bar(L::kBarUFull + s));
+    return u;
+  };
+  auto read_unit = [&](int r, bool warp_wide) -> int {
+    if (!a.dyn) return bwd_cta_unit(a, r);
+    const int s = r % L::kURing;
+    bool got = mbar_wait(bar(L::kBarUFull + s), (r / L::kURing) & 1, abort_flag);
+    if (warp_wide) got = __all_sync(0xffffffffu, got);
+    const int u = got ? uring[s] : -1;
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || lane == 0) mbar_arrive(bar(L::kBarUEmpty + s));
+    return u;
+  };
   auto unit_of = [&](int u) { return bwd_unit<kMod, kQB>(a, u, group); };
 
   if (warp == R::kTmaWarp) {
@@ -317,7 +357,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         }
         return true;
       };
-      for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+      for (int ri = 0, u = take_unit(0); ok && u >= 0; u = take_unit(++ri), ++unit) {
         const BwdUnit w = unit_of(u);
         // The unit's first block's Q / dO go out before its K / V: its stage
         // frees up while the previous unit still holds K and V, so it has landed
@@ -375,7 +415,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       constexpr bool dq_on_dp = (D == 64);
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+      for (int ri = 0, u = read_unit(0, false); ok && u >= 0; u = read_unit(++ri, false), ++unit) {
         const BwdUnit w = unit_of(u);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -527,7 +567,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     uint8_t* ds_rows = smem + L::kOffDS + r * 128;
     uint32_t it = 0;
     bool ok = true;
-    for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri)) {
+    for (int ri = 0, u = read_unit(0, true); ok && u >= 0; u = read_unit(++ri, true)) {
       const BwdUnit w = unit_of(u);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= w.kv_len;
@@ -637,7 +677,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
-    for (int ri = 0, u = next_unit(0); ok && u >= 0; u = next_unit(++ri), ++unit) {
+    for (int ri = 0, u = read_unit(0, true); ok && u >= 0; u = read_unit(++ri, true), ++unit) {
       const BwdUnit w = unit_of(u);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
@@ -891,6 +931,8 @@ static int launch_bwd_d(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
       const int rc = launch_bwd_main_pair(m, a, stream);
       if (rc != FA_OK) return rc;
     } else if (a.deterministic) {
+      BwdArgs am = a;
+      am.dyn = 0;  // (D = 128 deterministic calls run the 128-row kernel)
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
       cfg.blockDim = dim3(threads);
@@ -901,11 +943,16 @@ static int launch_bwd_d(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
       attr[0].val.cooperative = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, a) != cudaSuccess)
+      if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, am) != cudaSuccess)
         return FA_ERR_CUDA;
     } else {
+      // dynamic dealing at D = 128 with the snake (measured against the static
+      // snake at B2 H16 S8192 causal: 1,159 -> 1,173 TFLOP/s; at D = 64 it
+      // measured 1-4% slower and stays static)
+      BwdArgs am = a;
+      am.dyn = (D == 128) ? a.snake : 0;
       if (launch_pdl(kernel, dim3(grid), dim3(threads), L::kAllocBytes, stream, tq, tk, tv,
-                     tdo, a) != cudaSuccess)
+                     tdo, am) != cudaSuccess)
         return FA_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;

@@ -114,6 +114,13 @@ struct BwdArgs {
   int n_units;
   int snake;     // 1: units dealt longest-first (ascending kv tile) in a snake
   int desc;      // 1: each head's kv tiles dealt in descending order (deterministic mode)
+  // Dynamic dealing (bwd_main with the snake order): a CTA takes its next unit
+  // from an atomic counter, in an order that runs over groups of head_group kv
+  // heads, each group's longest units (lowest kv tile) first, so that the
+  // q / dO / dQ-accumulator lines of the heads in flight stay in L2
+  int dyn;
+  int head_group;
+  int* unit_counter;  // in the workspace header; cleared by the preprocess kernel
   // dQ accumulators: 1 in the atomic mode; in the deterministic mode kv tile j
   // adds into accumulator j % dq_groups, chained only behind tile j - dq_groups
   int dq_groups;
@@ -124,6 +131,9 @@ struct BwdArgs {
 };
 
 constexpr int kDetGroups = 4;       // deterministic-mode accumulators (at most)
+// L2 bytes the backward's dynamic dealing gives one group of kv heads (their
+// q, dO and dQ accumulators and K / V): about two groups are in flight at once
+constexpr double kBwdGroupBytes = 96.0 * (1 << 20);
 constexpr int kDetGroupsLong = 2;   // ... from kDetLongTiles kv tiles on
 constexpr int kDetLongTiles = 32;
 
