@@ -142,6 +142,19 @@ def test_bwd_workload_sampled_heads():
     _compare(det, ref, w, units)
 
 
+def test_bwd_head_groups_partial_last_group():
+    """Causal D=128 with atomic dQ deals its units from a counter over groups
+    of kv heads sized to L2: here 21 kv heads (B=3, Hkv=7, GQA 2, S=4096) in
+    groups of 9, 9 and 3.  kv heads at the group boundaries against the fp64
+    backward, every output finite."""
+    w = synth.Workload("head_groups", 3, 14, 7, 4096, 4096, 128, True, 12, with_do=True)
+    units = [0, 8, 9, 20]
+    got, ref, _ = _bwd_case(w, False, units=units)
+    _compare(got, ref, w, units)
+    for t in got:
+        assert bool(torch.isfinite(t.float()).all())
+
+
 @pytest.fixture
 def pair_kernel():
     prev = fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR)
