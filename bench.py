@@ -46,6 +46,8 @@ WORKLOAD = synth.BWD  # B=2, Hq=Hkv=16, S=8192, D=128, causal: the headline step
 SECONDARY = synth.TRAIN  # B=4, Hq=Hkv=16, S=2048, D=128, causal
 # the forward target: non-causal, D=128, S >= 8k (16k tokens per batch)
 LONG_FWD = [(8192, 128, False), (16384, 128, False), (32768, 128, False)]
+# the head-dimension-64 forward at S = 8k (its ring-of-score-buffers kernel)
+D64_FWD = [(8192, 64, False), (8192, 64, True)]
 NOMINAL_DENSE_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -485,6 +487,7 @@ def run_ours(args):
     # the forward target: non-causal D=128 at S >= 8k (16k tokens per batch)
     if rank == 0 and not args.no_long_fwd:
         extra["fwd_noncausal_long"] = fwd_sweep(fa, dev, peak, shapes=LONG_FWD)
+        extra["fwd_d64"] = fwd_sweep(fa, dev, peak, shapes=D64_FWD)
     if args.sweep and rank == 0:
         extra["fwd_sweep"] = fwd_sweep(fa, dev, peak)
     if args.mod_sweep and rank == 0:
@@ -797,7 +800,7 @@ def main(argv=None):
     ap.add_argument("--no-train-step", action="store_true",
                     help="skip the training-scale step reported under extra")
     ap.add_argument("--no-long-fwd", action="store_true",
-                    help="skip the non-causal S >= 8k forward reported under extra")
+                    help="skip the non-causal S >= 8k D=128 and the S = 8k D=64 forwards reported under extra")
     ap.add_argument("--only", default=None,
                     help="fwd:S:D:causal or bwd:S:D:causal[:det] -- time one kernel call "
                          "shape alone and exit")
