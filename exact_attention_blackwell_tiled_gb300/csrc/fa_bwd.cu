@@ -615,10 +615,15 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         {
           uint32_t v[kSC];
           tmem_ld<kSC>(t_row + s_col, v);
+          // s * c - LSE2 for two columns per packed FMA (same rounding as two fmaf)
+          const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
-          for (int c = 0; c < kSC; ++c) {
-            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, lse[c]));
-            p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x;
+          for (int c = 0; c < kSC; c += 2) {
+            const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
+                                         make_float2(lse[c], lse[c + 1]));
+            const float x0 = ex2_mufu(t2.x), x1 = ex2_mufu(t2.y);
+            p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x0;
+            p[c + 1] = (row_dead || c + 1 < c_lo || c + 1 > c_hi) ? 0.f : x1;
           }
         }
         {
@@ -630,11 +635,11 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         mbar_arrive(bar(L::kBarPReady + (it & 1)));
-        float dl[kSC];
+        float ndl[kSC];  // -Delta
 #pragma unroll
         for (int q = 0; q < kSC / 4; ++q) {
           const float4 x = s_delta[q];
-          dl[4 * q] = x.x, dl[4 * q + 1] = x.y, dl[4 * q + 2] = x.z, dl[4 * q + 3] = x.w;
+          ndl[4 * q] = -x.x, ndl[4 * q + 1] = -x.y, ndl[4 * q + 2] = -x.z, ndl[4 * q + 3] = -x.w;
         }
         if (!warp_wait_b(bar(L::kBarDPFull + it % L::kDPBufs), (it / L::kDPBufs) & 1, abort_flag)) {
           ok = false;
@@ -645,11 +650,15 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
         {
           uint32_t v[kSC];
           tmem_ld<kSC>(t_row + L::col_dp(it) + c0, v);
+          // dS = P (dP - Delta), two columns per packed add and multiply (the same
+          // roundings as the scalar form: a - b is a + (-b) exactly)
 #pragma unroll
           for (int e = 0; e < kSC / 2; ++e) {
-            const float d0 = p[2 * e] * (u2f(v[2 * e]) - dl[2 * e]);
-            const float d1 = p[2 * e + 1] * (u2f(v[2 * e + 1]) - dl[2 * e + 1]);
-            wbuf[e] = pack_bf16x2(d0, d1);
+            const float2 d = __fmul2_rn(
+                make_float2(p[2 * e], p[2 * e + 1]),
+                __fadd2_rn(make_float2(u2f(v[2 * e]), u2f(v[2 * e + 1])),
+                           make_float2(ndl[2 * e], ndl[2 * e + 1])));
+            wbuf[e] = pack_bf16x2(d.x, d.y);
           }
         }
         // dS^T over the second half of this warp's S^T columns (their S values
