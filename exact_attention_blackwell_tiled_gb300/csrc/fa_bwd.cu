@@ -617,13 +617,24 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
           tmem_ld<kSC>(t_row + s_col, v);
           // s * c - LSE2 for two columns per packed FMA (same rounding as two fmaf)
           const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+          if (!row_dead && c_lo <= 0 && c_hi >= kSC - 1) {
+            // every column of this thread's segment is visible (the common case)
 #pragma unroll
-          for (int c = 0; c < kSC; c += 2) {
-            const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
-                                         make_float2(lse[c], lse[c + 1]));
-            const float x0 = ex2_mufu(t2.x), x1 = ex2_mufu(t2.y);
-            p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x0;
-            p[c + 1] = (row_dead || c + 1 < c_lo || c + 1 > c_hi) ? 0.f : x1;
+            for (int c = 0; c < kSC; c += 2) {
+              const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
+                                           make_float2(lse[c], lse[c + 1]));
+              p[c] = ex2_mufu(t2.x);
+              p[c + 1] = ex2_mufu(t2.y);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kSC; c += 2) {
+              const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
+                                           make_float2(lse[c], lse[c + 1]));
+              const float x0 = ex2_mufu(t2.x), x1 = ex2_mufu(t2.y);
+              p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x0;
+              p[c + 1] = (row_dead || c + 1 < c_lo || c + 1 > c_hi) ? 0.f : x1;
+            }
           }
         }
         {
