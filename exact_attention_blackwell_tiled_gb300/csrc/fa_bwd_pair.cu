@@ -498,10 +498,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         {
           uint32_t v[kSC];
           tmem_ld<kSC>(t_row + s_col, v);
+          // two columns per packed FMA (the same rounding as two fmaf); no
+          // per-column mask when the whole segment is visible
+          const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+          const bool full = !row_dead && c_lo <= 0;
 #pragma unroll
-          for (int c = 0; c < kSC; ++c) {
-            const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, lse[c]));
-            p[c] = (row_dead || c < c_lo) ? 0.f : x;
+          for (int c = 0; c < kSC; c += 2) {
+            const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
+                                         make_float2(lse[c], lse[c + 1]));
+            const float x0 = ex2_mufu(t2.x), x1 = ex2_mufu(t2.y);
+            if (full) {
+              p[c] = x0;
+              p[c + 1] = x1;
+            } else {
+              p[c] = (row_dead || c < c_lo) ? 0.f : x0;
+              p[c + 1] = (row_dead || c + 1 < c_lo) ? 0.f : x1;
+            }
           }
         }
         {
@@ -528,8 +540,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_ld<kSC>(t_row + L::kColDP + c0, v);
 #pragma unroll
           for (int e = 0; e < kSC / 2; ++e) {
-            const float d0 = p[2 * e] * (u2f(v[2 * e]) - dl[2 * e]);
-            const float d1 = p[2 * e + 1] * (u2f(v[2 * e + 1]) - dl[2 * e + 1]);
+            // dS = P (dP - Delta), packed (the same roundings as the scalar form)
+            const float2 d2 = __fmul2_rn(
+                make_float2(p[2 * e], p[2 * e + 1]),
+                __fadd2_rn(make_float2(u2f(v[2 * e]), u2f(v[2 * e + 1])),
+                           make_float2(-dl[2 * e], -dl[2 * e + 1])));
+            const float d0 = d2.x, d1 = d2.y;
             wbuf[e] = pack_bf16x2(d0, d1);
           }
         }

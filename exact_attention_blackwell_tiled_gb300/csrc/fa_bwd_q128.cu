@@ -440,16 +440,29 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
         {
           uint32_t v[kSC];
           tmem_ld64(t_row + L::kColS + c0, v);
+          // s * c + bias - LSE2, two columns per packed FMA (the same rounding
+          // as two fmaf); no per-column mask when the whole segment is visible
+          const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+          const bool full = !row_dead && c_lo <= 0 && c_hi >= kSC - 1;
 #pragma unroll
           for (int q = 0; q < kSC / 4; ++q) {
             const float4 l4 = s_lse2[q];
             const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 4; e += 2) {
               const int c = 4 * q + e;
-              const float bias = kMod ? slope2 * (float)(kv - q0 - c) : 0.f;
-              const float x = ex2_mufu(fmaf(u2f(v[c]), a.scale_log2, bias - lq[e]));
-              p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x;
+              const float b0 = kMod ? slope2 * (float)(kv - q0 - c) : 0.f;
+              const float b1 = kMod ? slope2 * (float)(kv - q0 - c - 1) : 0.f;
+              const float2 t2 = __ffma2_rn(make_float2(u2f(v[c]), u2f(v[c + 1])), c2,
+                                           make_float2(b0 - lq[e], b1 - lq[e + 1]));
+              const float x0 = ex2_mufu(t2.x), x1 = ex2_mufu(t2.y);
+              if (full) {
+                p[c] = x0;
+                p[c + 1] = x1;
+              } else {
+                p[c] = (row_dead || c < c_lo || c > c_hi) ? 0.f : x0;
+                p[c + 1] = (row_dead || c + 1 < c_lo || c + 1 > c_hi) ? 0.f : x1;
+              }
             }
           }
         }
@@ -474,12 +487,19 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
           uint32_t wbuf[16];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
+            // dS = P (dP - Delta), two columns per packed add and multiply (the
+            // same roundings as the scalar form)
             const float4 d4 = s_delta[8 * h + q];
             const int c = 32 * h + 4 * q;
-            wbuf[2 * q] = pack_bf16x2(p[c] * (u2f(v[4 * q]) - d4.x),
-                                      p[c + 1] * (u2f(v[4 * q + 1]) - d4.y));
-            wbuf[2 * q + 1] = pack_bf16x2(p[c + 2] * (u2f(v[4 * q + 2]) - d4.z),
-                                          p[c + 3] * (u2f(v[4 * q + 3]) - d4.w));
+            const float2 s01 = __fmul2_rn(
+                make_float2(p[c], p[c + 1]),
+                __fadd2_rn(make_float2(u2f(v[4 * q]), u2f(v[4 * q + 1])), make_float2(-d4.x, -d4.y)));
+            const float2 s23 = __fmul2_rn(
+                make_float2(p[c + 2], p[c + 3]),
+                __fadd2_rn(make_float2(u2f(v[4 * q + 2]), u2f(v[4 * q + 3])),
+                           make_float2(-d4.z, -d4.w)));
+            wbuf[2 * q] = pack_bf16x2(s01.x, s01.y);
+            wbuf[2 * q + 1] = pack_bf16x2(s23.x, s23.y);
           }
           // dS^T over columns c0 + 32 + 16h .. +15 (their S^T values were read
           // in the P^T pass)
