@@ -42,7 +42,9 @@
 //               block into a 2-stage ring.
 //   warp 13     TMEM owner; one thread issues S^T, dV, dK and dQ^T.
 //   warp 14     one thread issues dP^T.
-//   warp 15     issues nothing (it completes the last warpgroup).
+//   warp 15     deterministic mode: one thread raises the dQ semaphores once
+//               the drain warps have added a block (so that no drain warp
+//               waits for its adds to reach L2).
 // Warps 12-15 run with 72 registers after the setmaxnreg split.
 #include <cuda_bf16.h>
 
@@ -84,7 +86,9 @@ struct Q128Layout {
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQEmpty + 1;
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
-  static constexpr int kBarDrain = kBarDKVEmpty + 1;  // 2: one per issuer
+  static constexpr int kBarDQAdded = kBarDKVEmpty + 1;    // drain warps -> semaphore warp
+  static constexpr int kBarDQAddedFree = kBarDQAdded + 1;  // semaphore warp -> drain warps
+  static constexpr int kBarDrain = kBarDQAddedFree + 1;    // 2: one per issuer
   static constexpr int kNumBars = kBarDrain + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
   static constexpr int kBytes = kOffMisc + 16;
@@ -97,7 +101,7 @@ struct Q128Layout {
   static constexpr int kTmaWarp = 12;
   static constexpr int kScoreWarp = 13;  // TMEM owner; S^T and gradient issuer
   static constexpr int kDPWarp = 14;     // dP^T issuer
-  static constexpr int kIdleWarp = 15;   // completes the issuers' warpgroup
+  static constexpr int kSemWarp = 15;    // raises the deterministic mode's semaphores
   static constexpr int kThreads = 512;
   static constexpr int kSmxThreads = 256;
   static constexpr int kRegsLaunch = 128;  // 65536 / kThreads
@@ -110,10 +114,10 @@ static_assert(2 * 128 * Q128Layout::kRegsLaunch + 128 * Q128Layout::kRegsDrain +
               "the register split must add up to the launch's registers");
 
 static_assert(Q128Layout::kDPWarp == Q128Layout::kScoreWarp + 1 &&
-                  Q128Layout::kIdleWarp == Q128Layout::kScoreWarp + 2 &&
-                  Q128Layout::kThreads == 32 * (Q128Layout::kIdleWarp + 1) &&
+                  Q128Layout::kSemWarp == Q128Layout::kScoreWarp + 2 &&
+                  Q128Layout::kThreads == 32 * (Q128Layout::kSemWarp + 1) &&
                   Q128Layout::kTmaWarp % 4 == 0,
-              "warps 12-15 (TMA, issuers) form the last warpgroup");
+              "warps 12-15 (TMA, issuers, semaphores) form the last warpgroup");
 
 // Shared memory the launch asks for: the layout plus whatever of the largest
 // opt-in size is left, for aligning the layout to 1024 bytes (the kernel checks
@@ -166,6 +170,8 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKVFull), 1);
     mbar_init(bar(L::kBarDKVEmpty), 128);
+    mbar_init(bar(L::kBarDQAdded), 4);  // lane 0 of each drain warp
+    mbar_init(bar(L::kBarDQAddedFree), 1);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarDrain + s), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -264,7 +270,8 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     // S^T(i+1) enters the tensor pipe right behind dK(i), the last reader of
     // S^T(i)'s columns, without waiting for dK(i) to complete (the MMAs of one
     // thread run in issue order), and ahead of dQ^T(i), whose result is not
-    // needed as soon.  Warp 14: dP^T.  Warp 15 issues nothing.
+    // needed as soon.  Warp 14: dP^T.  Warp 15 issues nothing; in the
+    // deterministic mode it raises the dQ semaphores.
     if (lane == 0 && warp <= L::kDPWarp) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kQB2, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, false, true);    // dV, dK
@@ -390,6 +397,32 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
       const int di = grad ? 0 : 1;
       umma_commit(bar(L::kBarDrain + di));
       drain_wait_b(bar(L::kBarDrain + di), 0);
+    }
+    if (lane == 0 && warp == L::kSemWarp && a.deterministic) {
+      // Block by block, once the four drain warps have added it (their
+      // arrives release at CTA scope what each warp's lanes added, and this
+      // wait acquires it), one add with release order at GPU scope moves the
+      // block's semaphore: whoever reads the new count sees the adds.  The
+      // drain warps go on to the next block meanwhile; the free barrier keeps
+      // them at most one block ahead of this thread.
+      uint32_t it = 0;
+      bool ok = true;
+      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
+        const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
+        const int g = w.j % a.dq_groups;
+        for (int t = 0; t < w.n_it; ++t, ++it) {
+          const int gi = t / w.n_blk;
+          const int iq = w.lo + (t - gi * w.n_blk);
+          const int bh = w.b * a.Hq + w.hk * group + gi;
+          if (!mbar_wait(bar(L::kBarDQAdded), it & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(bar(L::kBarDQAddedFree));
+          int* sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+        }
+      }
     }
   }
   } else if (warp < L::kSmxWarps) {
@@ -562,10 +595,10 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
                                           a.dq_groups)) / a.dq_groups;
           sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;
           if (turn > 0) {
-            // the semaphore counts the group's finished adding warps (4 per tile)
+            // the semaphore counts the group's tiles whose adds are done
             if (lane == 0) {
               const uint64_t t0 = global_timer_ns();
-              while (ld_acquire(sem) < turn * 4) {
+              while (ld_acquire(sem) < turn) {
                 if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
                   *abort_flag = 1;
                   good = 0;
@@ -592,11 +625,17 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
           }
         }
         if (a.deterministic && good) {
-          // the warp barrier orders every lane's adds before lane 0's release,
-          // which makes them visible before the count moves
+          // hand the block to the semaphore warp: the warp barrier orders every
+          // lane's adds before lane 0's arrive, which waits until the semaphore
+          // warp has taken the previous block (one barrier phase per block)
           __syncwarp();
-          if (lane == 0)
-            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+          if (lane == 0) {
+            if (it > 0 && !mbar_wait(bar(L::kBarDQAddedFree), (it - 1) & 1, abort_flag))
+              good = 0;
+            else
+              mbar_arrive(bar(L::kBarDQAdded));
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
         }
         ok = group_all(good != 0, 2);
         if (!ok) break;
