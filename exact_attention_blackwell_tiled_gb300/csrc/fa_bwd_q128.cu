@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKVFull), 1);
     mbar_init(bar(L::kBarDKVEmpty), 128);
-    mbar_init(bar(L::kBarDQAdded), 4);  // lane 0 of each drain warp
+    mbar_init(bar(L::kBarDQAdded), 128);  // every drain thread
     mbar_init(bar(L::kBarDQAddedFree), 1);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarDrain + s), 1);
     *abort_flag = 0;
@@ -399,12 +399,12 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
       drain_wait_b(bar(L::kBarDrain + di), 0);
     }
     if (lane == 0 && warp == L::kSemWarp && a.deterministic) {
-      // Block by block, once the four drain warps have added it (their
-      // arrives release at CTA scope what each warp's lanes added, and this
-      // wait acquires it), one add with release order at GPU scope moves the
-      // block's semaphore: whoever reads the new count sees the adds.  The
-      // drain warps go on to the next block meanwhile; the free barrier keeps
-      // them at most one block ahead of this thread.
+      // Block by block, once the drain threads have added it (each one's
+      // arrive releases at CTA scope what it added, and this wait acquires
+      // it), one add with release order at GPU scope moves the block's
+      // semaphore: whoever reads the new count sees the adds.  The drain warps
+      // go on meanwhile; the free barrier keeps them at most one block ahead
+      // of this thread.
       uint32_t it = 0;
       bool ok = true;
       for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
@@ -560,6 +560,20 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
+    // Deterministic mode: block it - 1's adds, handed to the semaphore warp
+    // only after block it's dQ^T has been read (or the unit's dK/dV are
+    // ready), so that the arrive, which orders this thread's adds before it
+    // (a release at CTA scope), does not hold the drain while they are still
+    // on their way to L2.  Each thread arrives for itself; the wait on the
+    // free barrier keeps the arrives one barrier phase per block.
+    bool handoff_due = false;
+    auto hand_off = [&]() -> bool {
+      if (!handoff_due) return true;
+      handoff_due = false;
+      if (it > 1 && !warp_wait_b(bar(L::kBarDQAddedFree), (it - 2) & 1, abort_flag)) return false;
+      mbar_arrive(bar(L::kBarDQAdded));
+      return true;
+    };
     for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
       const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
       for (int t = 0; t < w.n_it; ++t, ++it) {
@@ -578,7 +592,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
         tmem_ld128(t_row + L::kColDQ, v);
         tc_fence_before();
         mbar_arrive(bar(L::kBarDQEmpty));
-        int good = 1;
+        int good = hand_off() ? 1 : 0;
         int g = 0, turn = 0;
         int* sem = nullptr;
         if (a.deterministic) {
@@ -594,7 +608,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
                      : (w.j - group_first(qblk_first_contributor<kQB2>(win_left<kMod>(a), iq), g,
                                           a.dq_groups)) / a.dq_groups;
           sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;
-          if (turn > 0) {
+          if (good && turn > 0) {
             // the semaphore counts the group's tiles whose adds are done
             if (lane == 0) {
               const uint64_t t0 = global_timer_ns();
@@ -624,25 +638,16 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
                            : "memory");
           }
         }
-        if (a.deterministic && good) {
-          // hand the block to the semaphore warp: the warp barrier orders every
-          // lane's adds before lane 0's arrive, which waits until the semaphore
-          // warp has taken the previous block (one barrier phase per block)
-          __syncwarp();
-          if (lane == 0) {
-            if (it > 0 && !mbar_wait(bar(L::kBarDQAddedFree), (it - 1) & 1, abort_flag))
-              good = 0;
-            else
-              mbar_arrive(bar(L::kBarDQAdded));
-          }
-          good = __shfl_sync(0xffffffffu, good, 0);
-        }
+        if (a.deterministic && good) handoff_due = true;
         ok = group_all(good != 0, 2);
         if (!ok) break;
       }
       if (!ok) break;
       // ---- dK, dV epilogue for key row kv
-      ok = group_all(warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag), 2);
+      {
+        const bool ready = warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag);
+        ok = group_all(hand_off() && ready, 2);  // the unit's last block, it - 1
+      }
       if (!ok) break;
       tc_fence_after();
       // Each thread holds one key row; to store whole 64-byte row pieces per
