@@ -39,7 +39,9 @@
 //               after a setmaxnreg split) and the dK/dV epilogue at the end of
 //               a unit.
 //   warp 12     TMA producer: K_j, V_j per unit; Q_i, dO_i, LSE2_i, Delta_i per
-//               block into a 2-stage ring.
+//               block into a 2-stage ring.  With dynamic dealing (the
+//               deterministic mode with the snake order) it also takes each
+//               unit number from the global counter.
 //   warp 13     TMEM owner; one thread issues S^T, dV, dK and dQ^T.
 //   warp 14     one thread issues dP^T.
 //   warp 15     deterministic mode: one thread raises the dQ semaphores once
@@ -89,9 +91,13 @@ struct Q128Layout {
   static constexpr int kBarDQAdded = kBarDKVEmpty + 1;    // drain warps -> semaphore warp
   static constexpr int kBarDQAddedFree = kBarDQAdded + 1;  // semaphore warp -> drain warps
   static constexpr int kBarDrain = kBarDQAddedFree + 1;    // 2: one per issuer
-  static constexpr int kNumBars = kBarDrain + 2;
+  static constexpr int kURing = 8;  // dynamically dealt units posted by the TMA thread
+  static constexpr int kBarUFull = kBarDrain + 2;        // kURing
+  static constexpr int kBarUEmpty = kBarUFull + kURing;  // kURing
+  static constexpr int kNumBars = kBarUEmpty + kURing;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kOffURing = kOffMisc + 16;
+  static constexpr int kBytes = kOffURing + 4 * kURing;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
   // warp roles
@@ -173,6 +179,12 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     mbar_init(bar(L::kBarDQAdded), 128);  // every drain thread
     mbar_init(bar(L::kBarDQAddedFree), 1);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarDrain + s), 1);
+    // readers of a posted unit: the softmax and drain warps, both issuing
+    // threads and, in the deterministic mode, the semaphore thread
+    for (int s = 0; s < L::kURing; ++s) {
+      mbar_init(bar(L::kBarUFull + s), 1);
+      mbar_init(bar(L::kBarUEmpty + s), L::kSmxWarps + 4 + 2 + (a.deterministic ? 1 : 0));
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -195,6 +207,32 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
   grid_dep_launch();
   const uint32_t tmem = *tmem_slot;
   const int group = a.Hq / a.Hkv;
+  // The r-th unit of this CTA: static dealing computes it in every role;
+  // dynamic dealing has the TMA thread take the next number from the global
+  // counter and post it in ring slot r % kURing, where the other roles read it.
+  // Units are taken in dealing order, so a tile still waits only for tiles
+  // taken before it.
+  volatile int* uring = reinterpret_cast<volatile int*>(smem + L::kOffURing);
+  auto take_unit = [&](int r) -> int {
+    if (!a.dyn) return bwd_cta_unit(a, r);
+    const int s = r % L::kURing;
+    if (!mbar_wait(bar(L::kBarUEmpty + s), ((r / L::kURing) & 1) ^ 1, abort_flag)) return -1;
+    int u = atomicAdd(a.unit_counter, 1);
+    if (u >= a.n_units) u = -1;
+    uring[s] = u;
+    mbar_arrive(bar(L::kBarUFull + s));
+    return u;
+  };
+  auto read_unit = [&](int r, bool warp_wide) -> int {
+    if (!a.dyn) return bwd_cta_unit(a, r);
+    const int s = r % L::kURing;
+    bool got = mbar_wait(bar(L::kBarUFull + s), (r / L::kURing) & 1, abort_flag);
+    if (warp_wide) got = __all_sync(0xffffffffu, got);
+    const int u = got ? uring[s] : -1;
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || lane == 0) mbar_arrive(bar(L::kBarUEmpty + s));
+    return u;
+  };
   // Register split (512 threads x 128 at launch): the TMA / issuer warpgroup
   // gives up 56 per thread, the drain warpgroup takes them, so that a drain
   // thread holds its whole 128-column row of dQ^T and releases the columns
@@ -226,7 +264,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
         }
         return true;
       };
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
+      for (int ri = 0, u = take_unit(0); ok && u >= 0; u = take_unit(++ri), ++unit) {
         const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
         // the unit's first block's Q / dO go out before its K / V: that stage
         // frees while the previous unit still holds K and V
@@ -292,7 +330,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
       };
       uint32_t it = 0, unit = 0;
       bool ok = true;
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
+      for (int ri = 0, u = read_unit(0, false); ok && u >= 0; u = read_unit(++ri, false), ++unit) {
         const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
         if (!mbar_wait(bar(L::kBarKVFull), unit & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
       // of this thread.
       uint32_t it = 0;
       bool ok = true;
-      for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
+      for (int ri = 0, u = read_unit(0, false); ok && u >= 0; u = read_unit(++ri, false)) {
         const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
         const int g = w.j % a.dq_groups;
         for (int t = 0; t < w.n_it; ++t, ++it) {
@@ -438,7 +476,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
     const int wl = win_left<kMod>(a), wr = win_right<kMod>(a);
     uint32_t it = 0;
     bool ok = true;
-    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri)) {
+    for (int ri = 0, u = read_unit(0, true); ok && u >= 0; u = read_unit(++ri, true)) {
       const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
       const int kv = w.j * kTile + r;
       const bool row_dead = kv >= w.kv_len;
@@ -577,7 +615,7 @@ __global__ void __launch_bounds__(Q128Layout::kThreads, 1)
       mbar_arrive(bar(L::kBarDQAdded));
       return true;
     };
-    for (int ri = 0, u = bwd_cta_unit(a, 0); ok && u >= 0; u = bwd_cta_unit(a, ++ri), ++unit) {
+    for (int ri = 0, u = read_unit(0, true); ok && u >= 0; u = read_unit(++ri, true), ++unit) {
       const BwdUnit w = bwd_unit<kMod, kQB2>(a, u, group);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
