@@ -225,9 +225,13 @@ struct BwdSmem {
   static constexpr int kBarDKVEmpty = kBarDKVFull + 1;
   static constexpr int kBarSFree = kBarDKVEmpty + 1;   // 2: S^T buffer read by dV and dK
   static constexpr int kBarDrain = kBarSFree + 2;      // 3: one per issuer
+  // deterministic mode at D = 64: drain warps 0-1 hand each block they have
+  // added to lane 0 of drain warp 2, which raises the block's semaphore
+  static constexpr int kBarDQAdded = kBarDrain + 3;       // (D = 64 only)
+  static constexpr int kBarDQAddedFree = kBarDQAdded + 1;
   // dynamic dealing: a ring of unit numbers taken by the TMA thread
   static constexpr int kURing = 8;
-  static constexpr int kBarUFull = kBarDrain + 3;      // kURing
+  static constexpr int kBarUFull = kBarDrain + 3 + (D < 128 ? 2 : 0);  // kURing
   static constexpr int kBarUEmpty = kBarUFull + kURing;  // kURing
   static constexpr int kNumBars = kBarUEmpty + kURing;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
@@ -280,7 +284,13 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     }
     for (int s = 0; s < L::kDPBufs; ++s) mbar_init(bar(L::kBarDPFull + s), 1);
     mbar_init(bar(L::kBarDQFull), 1);
-    mbar_init(bar(L::kBarDQEmpty), 128);
+    // the drain threads that read dQ^T: all 128, but in the deterministic mode
+    // at D = 64 only drain warps 0-1, which hold its head-dim rows
+    mbar_init(bar(L::kBarDQEmpty), (D < 128 && a.deterministic) ? D : 128);
+    if (D < 128) {
+      mbar_init(bar(L::kBarDQAdded), D);
+      mbar_init(bar(L::kBarDQAddedFree), 1);
+    }
     mbar_init(bar(L::kBarDKVFull), 1);
     mbar_init(bar(L::kBarDKVEmpty), 128);
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kBarSFree + s), 1);
@@ -700,19 +710,57 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t it = 0, unit = 0;
     bool ok = true;
+    constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
+    // D = 64: the other two drain warps read no dQ^T; in the deterministic
+    // mode lane 0 of the first of them raises the semaphores (below)
+    constexpr bool kSemWarp = kAddWarps < 4;
+    // Deterministic mode with the semaphore warp: block it - 1's adds are
+    // handed over only once block it's dQ^T is complete (or the unit's dK/dV
+    // are), so that the arrive, which orders this thread's adds before it (a
+    // release at CTA scope), does not hold the drain while they are on their
+    // way to L2.  The free barrier keeps the arrives one phase per block.
+    bool handoff_due = false;
+    auto hand_off = [&]() -> bool {
+      if (!handoff_due) return true;
+      handoff_due = false;
+      if (it > 1 && !warp_wait_b(bar(L::kBarDQAddedFree), (it - 2) & 1, abort_flag)) return false;
+      mbar_arrive(bar(L::kBarDQAdded));
+      return true;
+    };
     for (int ri = 0, u = read_unit(0, true); ok && u >= 0; u = read_unit(++ri, true), ++unit) {
       const BwdUnit w = unit_of(u);
       for (int t = 0; t < w.n_it; ++t, ++it) {
         const int gi = t / w.n_blk;
         const int iq = w.lo + (t - gi * w.n_blk);
         const int bh = w.b * a.Hq + w.hk * group + gi;
+        if (kSemWarp && a.deterministic && wq >= kAddWarps) {
+          if (wq == kAddWarps) {
+            // once drain warps 0-1 have added block it (their arrives release
+            // at CTA scope what each thread added, this wait acquires it), one
+            // add with release order at GPU scope moves its semaphore
+            int good = 1;
+            if (lane == 0) {
+              if (!mbar_wait(bar(L::kBarDQAdded), it & 1, abort_flag)) {
+                good = 0;
+              } else {
+                mbar_arrive(bar(L::kBarDQAddedFree));
+                int* sem = a.sem + (size_t)(w.j % a.dq_groups) * a.sem_group_stride +
+                           (size_t)bh * a.n_qblk + iq;
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            if (!ok) break;
+          }
+          continue;
+        }
         ok = warp_wait_b(bar(L::kBarDQFull), it & 1, abort_flag);
+        if (ok && kSemWarp && a.deterministic) ok = hand_off();
         if (!ok) break;
         tc_fence_after();
         // Row r of dQ^T (head-dim index r, 64 queries) goes straight from TMEM
         // to the fp32 accumulator: for each query the 32 lanes of a warp add
         // 32 consecutive floats, one 128-byte line per instruction.
-        constexpr int kAddWarps = D / 32;  // warps whose lanes hold real head-dim rows
         int good = 1;
         if (!a.deterministic) {
           // two 32-column halves, so that only 32 values are live at a time;
@@ -752,10 +800,11 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
                        ((size_t)bh * a.Sq_pad + (size_t)iq * kQB) * D + r;
           int* sem = a.sem + (size_t)g * a.sem_group_stride + (size_t)bh * a.n_qblk + iq;
           if (wq < kAddWarps && turn > 0) {
-            // the semaphore counts the group's finished adding warps
+            // the semaphore counts the group's finished adding warps (with
+            // the semaphore warp: the group's finished tiles)
             if (lane == 0) {
               const uint64_t t0 = global_timer_ns();
-              while (ld_acquire(sem) < turn * kAddWarps) {
+              while (ld_acquire(sem) < turn * (kSemWarp ? 1 : kAddWarps)) {
                 if (*abort_flag || global_timer_ns() - t0 > kWaitTimeoutNs) {
                   *abort_flag = 1;
                   good = 0;
@@ -789,11 +838,15 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
             }
           }
           if (wq < kAddWarps && good) {
-            // the warp barrier orders every lane's adds before lane 0's
-            // release, which makes them visible before the count moves
-            __syncwarp();
-            if (lane == 0)
-              asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+            if (kSemWarp) {
+              handoff_due = true;
+            } else {
+              // the warp barrier orders every lane's adds before lane 0's
+              // release, which makes them visible before the count moves
+              __syncwarp();
+              if (lane == 0)
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+            }
           }
         }
         ok = good != 0;
@@ -802,6 +855,7 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
       if (!ok) break;
       // ---- dK, dV epilogue for key row kv
       ok = warp_wait_b(bar(L::kBarDKVFull), unit & 1, abort_flag);
+      if (kSemWarp && wq < kAddWarps && !hand_off()) ok = false;  // the unit's last block
       if (!ok) break;
       tc_fence_after();
       // Each thread holds one key row; to store whole 64-byte row pieces per
@@ -963,7 +1017,12 @@ static int launch_bwd_d(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
       if (rc != FA_OK) return rc;
     } else if (a.deterministic) {
       BwdArgs am = a;
-      am.dyn = 0;  // (D = 128 deterministic calls run the 128-row kernel)
+      // (D = 128 deterministic calls run the 128-row kernel.)  With the snake
+      // order, units come from the global counter over all heads, in the
+      // snake's order (D = 64, B2 H16 S8192 causal: 369 -> 393 TFLOP/s
+      // against the static snake)
+      am.dyn = a.snake;
+      am.head_group = a.B * a.Hkv;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
       cfg.blockDim = dim3(threads);
