@@ -103,6 +103,11 @@ DET_WORKLOADS = [
     (synth.BWD, True),
     # non-causal: head-major dealing, chains descending
     (synth.BWD.with_(name="bwd_noncausal", causal=False), False),
+    # D = 64 runs the 64-row kernel, where a drain warp without head-dim rows
+    # raises the semaphores: causal (units from the global counter) and
+    # non-causal (static head-major dealing)
+    (synth.BWD.with_(name="bwd_d64", D=64), True),
+    (synth.BWD.with_(name="bwd_d64_noncausal", D=64, causal=False), False),
 ]
 
 
