@@ -520,6 +520,7 @@ def run_only(fa, args, dev):
       --only fwd:S:D:causal             the forward on the sweep workload of that S, D
       --only bwd:S:D:causal[:det|:pair] the backward on it: atomic dQ, deterministic dQ,
                                         or atomic on the CTA-pair kernel
+      --only-batch B                    that shape with batch B instead
     """
     import torch
     parts = args.only.split(":")
@@ -531,6 +532,8 @@ def run_only(fa, args, dev):
     if mode == "pair":
         fa.set_bwd_kernel(fa.BWD_KERNEL_PAIR)
     w = synth.sweep(int(S), int(D), c in ("1", "c", "causal", "true"))
+    if args.only_batch:
+        w = w.with_(B=args.only_batch)
     gen = torch.Generator(device=dev).manual_seed(w.seed)
     q, k, v, do = (torch.randn(w.B, w.Hq, w.Sq, w.D, device=dev, generator=gen).to(torch.bfloat16)
                    for _ in range(4))
@@ -804,6 +807,9 @@ def main(argv=None):
     ap.add_argument("--only", default=None,
                     help="fwd:S:D:causal or bwd:S:D:causal[:det] -- time one kernel call "
                          "shape alone and exit")
+    ap.add_argument("--only-batch", type=int, default=0,
+                    help="with --only: the batch size instead of the sweep's (e.g. 4 at S=2048 "
+                         "for the training-scale shape B4 H16 S2048)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
