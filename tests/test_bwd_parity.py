@@ -151,13 +151,23 @@ def test_bwd_head_groups_partial_last_group():
     """Causal D=128 with atomic dQ deals its units from a counter over groups
     of kv heads sized to L2: here 21 kv heads (B=3, Hkv=7, GQA 2, S=4096) in
     groups of 9, 9 and 3.  kv heads at the group boundaries against the fp64
-    backward, every output finite."""
+    backward, every output finite; then the deterministic mode on the same
+    shape."""
     w = synth.Workload("head_groups", 3, 14, 7, 4096, 4096, 128, True, 12, with_do=True)
     units = [0, 8, 9, 20]
-    got, ref, _ = _bwd_case(w, False, units=units)
+    got, ref, args = _bwd_case(w, False, units=units)
     _compare(got, ref, w, units)
     for t in got:
         assert bool(torch.isfinite(t.float()).all())
+    # the deterministic mode on the same GQA shape: units from the counter over
+    # all 21 kv heads, two query heads per unit behind the semaphore chain;
+    # against the fp64 backward and bit-identical on a second run
+    qd, kd, vd, o, dod, lse, _ = args
+    det = fa.bwd(qd, kd, vd, o, dod, lse, causal=True, scale=w.softmax_scale, deterministic=True)
+    _compare(det, ref, w, units)
+    again = fa.bwd(qd, kd, vd, o, dod, lse, causal=True, scale=w.softmax_scale, deterministic=True)
+    for a, b in zip(det, again):
+        assert torch.equal(a, b), "deterministic backward differs between runs"
 
 
 @pytest.fixture
