@@ -1001,14 +1001,16 @@ static int launch_bwd_d(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
         (mod || D == 64) ? BwdRoles<true>::kThreads : BwdRoles<false>::kThreads;
     record_timing(false, stream);
     if (a.qblk_rows == 128) {
-      // the deterministic mode with the snake order deals units from the
-      // global counter, over all heads in that same order (measured at B2 H16
-      // S8192 causal: 899 -> 986 TFLOP/s against the static snake; a CTA
-      // whose unit waited on the semaphore chain takes its next unit later
-      // instead of holding one dealt in advance)
+      // the deterministic mode deals units from the global counter in the
+      // static order: the snake's over all heads, or head-major (groups of one
+      // kv head, each head's tiles highest first).  Measured against static
+      // dealing: B2 H16 S8192 causal 899 -> 986 TFLOP/s, non-causal 889 -> 904,
+      // B8 H16 S2048 non-causal 829 -> 850; a CTA whose unit waited on the
+      // semaphore chain takes its next unit later instead of holding one dealt
+      // in advance
       BwdArgs aq = a;
-      aq.dyn = (a.deterministic && a.snake) ? 1 : 0;
-      aq.head_group = a.B * a.Hkv;
+      aq.dyn = a.deterministic ? 1 : 0;
+      aq.head_group = a.snake ? a.B * a.Hkv : 1;
       const int rc = launch_bwd_main_q128(tq, tk, tv, tdo, aq, mod, grid, stream);
       if (rc != FA_OK) return rc;
     } else if (g_bwd_kernel.load(std::memory_order_relaxed) == FA_BWD_KERNEL_PAIR &&
