@@ -49,9 +49,10 @@ def _noalloc(q, k, v, o, do, lse, dq, dk, dv, w, deterministic):
                                    float(w.softmax_scale), int(deterministic), _stream())
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("deterministic", [False, True], ids=["atomic", "det"])
-def test_noalloc_matches_oracle_and_fa_bwd_twice(deterministic):
-    w = synth.Workload("noalloc", 2, 4, 2, 300, 300, 128, True, 17, with_do=True)
+def test_noalloc_matches_oracle_and_fa_bwd_twice(deterministic, D):
+    w = synth.Workload("noalloc", 2, 4, 2, 300, 300, D, True, 17, with_do=True)
     qh, kh, vh, doh = synth.make_inputs(w, with_do=True)
     q, k, v, do = (t.to(DEV) for t in (qh, kh, vh, doh))
     o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.softmax_scale)
