@@ -776,11 +776,19 @@ __global__ void __launch_bounds__(BwdRoles<kMod || D == 64>::kThreads, 1)
             }
             if (r < D) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
+              for (int e = 0; e < 32; ++e) {
                 asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(
                                  dst + (size_t)(hf * 32 + e) * D),
                              "f"(u2f(v[e]))
                              : "memory");
+                // D = 128: a pause after every eight adds spreads a block's
+                // adds over its period; issued in one burst, they hold up the
+                // shared-memory and barrier operations of the softmax warps
+                // on the same SM sub-partitions (measured: +2.2% at B2 H16
+                // S8192 causal, +2.5% at B4 H16 S2048; at D = 64, whose blocks
+                // are shorter, the drain then falls behind: -11%)
+                if (D == 128 && (e & 7) == 7) __nanosleep(16);
+              }
             }
           }
         } else {
